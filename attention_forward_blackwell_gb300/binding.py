@@ -1,0 +1,161 @@
+"""ctypes binding of libfa_gb300.so (argument marshalling only).
+
+Every function here checks tensor shapes/dtypes/devices, allocates outputs with
+torch when the caller does not pass them, and calls the C ABI declared in
+``include/fa.h`` on the current torch CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; there is no fallback path.  If the library has not
+been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_MISALIGNED, FA_ERR_CUDA, \
+    FA_ERR_TIMEOUT = range(6)
+FA_DECODE_MAX_SQ = 16
+
+# name -> (restype, argtypes); must match include/fa.h
+_VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+_FWD = [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _F, _I]
+SIGNATURES = {
+    "fa_fwd_prefill": (_I, _FWD + [_VP]),
+    "fa_fwd_decode": (_I, _FWD + [_VP]),
+    "fa_fwd_decode_splits": (_I, _FWD + [_I, _VP]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_get_device_error": (_I, [_VP]),
+    "fa_get_device_error_word": (_I, [_VP, ctypes.POINTER(ctypes.c_uint)]),
+    "fa_selftest_wait_timeout": (_I, [_LL, _VP]),
+    "fa_version": (_I, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} ({status})")
+
+
+def lib(path: str | None = None):
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it with attention_forward_blackwell_gb300."
+                    "build.build() (there is no CPU fallback)")
+            handle = ctypes.CDLL(p)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return lib().fa_version()
+
+
+def _stream_ptr(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check_inputs(q, k, v, seqlens_k):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16")
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, Hq, Sq, d = q.shape
+    Bk, Hkv, Sk, dk = k.shape
+    if v.shape != k.shape or Bk != B or dk != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if seqlens_k is not None:
+        if seqlens_k.dtype != torch.int32 or not seqlens_k.is_cuda or seqlens_k.shape != (B,):
+            raise ValueError("seqlens_k must be a CUDA int32 tensor of shape [B]")
+        seqlens_k = seqlens_k.contiguous()
+    return B, Hq, Hkv, Sq, Sk, d, seqlens_k
+
+
+def _outputs(q, out, lse):
+    B, Hq, Sq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, Hq, Sq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor of shape [B, Hq, Sq]")
+    return out, lse
+
+
+def prefill(q, k, v, scale=None, causal=False, seqlens_k=None, out=None, lse=None,
+            stream=None):
+    """Attention forward through ``fa_fwd_prefill``; returns (o, lse)."""
+    B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
+    out, lse = _outputs(q, out, lse)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().fa_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                              Sq, Sk, _ptr(seqlens_k), d, scale, int(bool(causal)),
+                              _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_prefill")
+    return out, lse
+
+
+def decode(q, k, v, scale=None, causal=False, seqlens_k=None, num_splits=0, out=None,
+           lse=None, stream=None):
+    """Split-KV attention forward through ``fa_fwd_decode_splits``
+    (num_splits <= 0 lets the library choose, as ``fa_fwd_decode`` does)."""
+    B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
+    out, lse = _outputs(q, out, lse)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk,
+            _ptr(seqlens_k), d, scale, int(bool(causal)))
+    if num_splits and num_splits > 0:
+        st = lib().fa_fwd_decode_splits(*args, int(num_splits), _stream_ptr(stream))
+    else:
+        st = lib().fa_fwd_decode(*args, _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_decode")
+    return out, lse
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and read/clear the device error word."""
+    return lib().fa_get_device_error(_stream_ptr(stream))
+
+
+def get_device_error_word(stream=None):
+    """(status, raw error word) after synchronising the stream; clears it."""
+    w = ctypes.c_uint(0)
+    st = lib().fa_get_device_error_word(_stream_ptr(stream), ctypes.byref(w))
+    return st, w.value
+
+
+def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return lib().fa_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))

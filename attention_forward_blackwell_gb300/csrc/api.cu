@@ -1,0 +1,298 @@
+// C ABI of libfa_gb300.so (declared in include/fa.h): argument validation,
+// device checks, TMA tensor-map encoding, split planning and kernel dispatch.
+// Everything runs on the host and only enqueues work on the caller's stream.
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "common.cuh"
+
+namespace fa {
+namespace {
+
+// Device error word written by kernels whose bounded waits give up.
+__device__ unsigned int g_err_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int* err_word = nullptr;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Looks up (once) the properties of the current device.  Returns nullptr if
+// the CUDA runtime fails.
+const DeviceInfo* device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& di = g_dev[dev];
+    if (!di.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        di.supported = (major == 10 && minor == 3);
+        di.num_sms = sms;
+        if (di.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return nullptr;
+            di.err_word = static_cast<unsigned int*>(p);
+            // keep stream-ordered workspace blocks cached between calls
+            cudaMemPool_t pool;
+            if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+                uint64_t thr = UINT64_MAX;
+                cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+            }
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return nullptr;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        di.ready = true;
+    }
+    return &di;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 3-D bf16 tensor map over [planes][rows][d] with a {64, 128, 1} box and
+// 128-byte swizzle (rows past `rows` and columns past `d` read as zero).
+bool encode_map(CUtensorMap* m, const void* base, int d, int rows, long long planes) {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Common {
+    bool noop = false;   // nothing to compute
+};
+
+// Checks shared by prefill and decode; fills `c.noop`.
+fa_status check_common(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int batch, int hq, int hkv, int sq, int sk, float scale, Common& c) {
+    if (batch < 0 || hq < 0 || hkv < 0 || sq < 0 || sk < 0) return FA_ERR_INVALID_ARG;
+    if (batch > 65535 || hq > 65535) return FA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+    if (batch == 0 || hq == 0 || sq == 0) {
+        c.noop = true;
+        return FA_OK;
+    }
+    if (hkv == 0 || hq % hkv != 0) return FA_ERR_INVALID_ARG;
+    if (!q || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (sk > 0 && (!k || !v)) return FA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || (sk > 0 && (!aligned16(k) || !aligned16(v))))
+        return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
+fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
+
+fa_status decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                      int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
+                      float scale, int causal, int num_splits, fa_stream_t stream) {
+    Common c;
+    fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
+    if (st != FA_OK || c.noop) return st;
+    if (sq > FA_DECODE_MAX_SQ) return FA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return FA_ERR_UNSUPPORTED;
+    const long long q_elems = (long long)batch * hq * sq * head_dim;
+    if (q_elems >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (sk == 0)
+        return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
+                                           (long long)batch * hq * sq, head_dim, s));
+
+    DecodeArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.k = static_cast<const uint16_t*>(k);
+    a.v = static_cast<const uint16_t*>(v);
+    a.o = static_cast<uint16_t*>(o);
+    a.lse = lse;
+    a.seqlens_k = seqlens_k;
+    a.B = batch;
+    a.Hq = hq;
+    a.Hkv = hkv;
+    a.Sq = sq;
+    a.Sk = sk;
+    a.group = hq / hkv;
+    a.rows = a.group * sq;
+    a.n_mtiles = (a.rows + 15) / 16;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    if ((long long)hkv * a.n_mtiles > 65535) return FA_ERR_INVALID_ARG;
+    // split planning: equal chunks of a multiple of 64 keys
+    int splits = num_splits;
+    if (splits <= 0) {
+        const long long pairs = (long long)batch * hkv * a.n_mtiles;
+        const long long target = 8ll * di->num_sms;    // CTAs worth keeping in flight
+        long long want = (target + pairs - 1) / pairs;
+        const long long max_splits = (sk + 255) / 256;  // at least 256 keys per split
+        if (want > max_splits) want = max_splits;
+        if (want < 1) want = 1;
+        splits = (int)want;
+    }
+    long long chunk = ((long long)sk + splits - 1) / splits;
+    chunk = (chunk + 63) / 64 * 64;
+    a.chunk = (int)chunk;
+    a.n_splits = (int)((sk + chunk - 1) / chunk);
+    const size_t rows = (size_t)batch * hq * sq;
+    const size_t bytes_o = (size_t)a.n_splits * rows * head_dim * sizeof(float);
+    const size_t bytes_l = (size_t)a.n_splits * rows * sizeof(float);
+    void* ws = nullptr;
+    if (cudaMallocAsync(&ws, bytes_o + bytes_l, s) != cudaSuccess) return FA_ERR_CUDA;
+    a.part_o = static_cast<float*>(ws);
+    a.part_lse = reinterpret_cast<float*>(static_cast<char*>(ws) + bytes_o);
+    cudaError_t e = launch_decode(a, head_dim, s);
+    cudaError_t ef = cudaFreeAsync(ws, s);
+    if (e != cudaSuccess || ef != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                         int head_dim, float scale, int causal, fa_stream_t stream) {
+    Common c;
+    fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
+    if (st != FA_OK || c.noop) return st;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
+        return FA_ERR_UNSUPPORTED;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (sk == 0)
+        return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
+                                           (long long)batch * hq * sq, head_dim, s));
+    PrefillLaunch p;
+    if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
+        !encode_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv) ||
+        !encode_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv) ||
+        !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
+        return FA_ERR_INVALID_ARG;
+    PrefillArgs& a = p.args;
+    a.lse = lse;
+    a.seqlens_k = seqlens_k;
+    a.err_word = di->err_word;
+    a.B = batch;
+    a.Hq = hq;
+    a.Hkv = hkv;
+    a.Sq = sq;
+    a.Sk = sk;
+    a.group = hq / hkv;
+    const int rows_per_cta = prefill_rows_per_cta(head_dim);
+    a.num_mblk = (sq + rows_per_cta - 1) / rows_per_cta;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.wait_limit_ns = kWaitLimitNs;
+    p.head_dim = head_dim;
+    p.causal = causal ? 1 : 0;
+    cudaError_t e;
+    switch (head_dim) {
+        case 64: e = launch_prefill_d64(p, s); break;
+        case 96: e = launch_prefill_d96(p, s); break;
+        case 128: e = launch_prefill_d128(p, s); break;
+        default: e = launch_prefill_d256(p, s); break;
+    }
+    return from_cuda(e);
+}
+
+fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                        int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                        int head_dim, float scale, int causal, fa_stream_t stream) {
+    return decode_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                       causal, 0, stream);
+}
+
+fa_status fa_fwd_decode_splits(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                               int head_dim, float scale, int causal, int num_splits,
+                               fa_stream_t stream) {
+    return decode_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                       causal, num_splits, stream);
+}
+
+const char* fa_status_string(fa_status status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+fa_status fa_get_device_error(fa_stream_t stream) {
+    return fa_get_device_error_word(stream, nullptr);
+}
+
+fa_status fa_get_device_error_word(fa_stream_t stream, unsigned int* word_out) {
+    if (word_out) *word_out = 0;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FA_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, di->err_word, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (word_out) *word_out = word;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(di->err_word, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+            return FA_ERR_CUDA;
+        return FA_ERR_TIMEOUT;
+    }
+    return FA_OK;
+}
+
+fa_status fa_selftest_wait_timeout(long long limit_ns, fa_stream_t stream) {
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    if (limit_ns < 1000) limit_ns = 1000;
+    if (limit_ns > 1000000000ll) limit_ns = 1000000000ll;
+    return from_cuda(launch_wait_timeout_selftest(di->err_word, (unsigned long long)limit_ns,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

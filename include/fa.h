@@ -1,0 +1,149 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libfa_gb300.so).
+ *
+ * The library computes, for every batch entry b, query head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j  over visible j) * v_j
+ *     LSE[b,h,i] = ln sum_{visible j} exp(scale * q_i . k_j)
+ *
+ * ("b200-flash-attention4-planner", section E step 1 fixes these semantics:
+ * shapes, layout, head_dim, causal, GQA ratio, scale, output and LSE; its
+ * section A1 "Streaming online softmax" is the tile-by-tile method the
+ * kernels use: running row_max / row_sum, O rebased when the max grows,
+ * divided by row_sum only at the end).
+ *
+ * Conventions shared by every entry point below:
+ *   Layout    q, o : [batch, hq,  sq, head_dim]  bf16, contiguous (row-major)
+ *             k, v : [batch, hkv, sk, head_dim]  bf16, contiguous
+ *             lse  : [batch, hq,  sq]            fp32, contiguous
+ *             bf16 is passed as raw 16-bit patterns.
+ *   Pointers  q, k, v, o, lse and seqlens_k are DEVICE pointers of the
+ *             current CUDA device.  All buffers are owned by the caller; the
+ *             library neither frees nor retains them after the call returns.
+ *             q, k, v and o must be 16-byte aligned (TMA requirement).
+ *   GQA       hq must be a multiple of hkv; query head h reads key/value head
+ *             h / (hq / hkv) (consecutive query heads share a key/value head).
+ *   Lengths   seqlens_k: device int32[batch] of valid key counts L_b, or NULL
+ *             (then L_b = sk).  Values are clamped to [0, sk] on the device.
+ *             Key/value rows j >= L_b are never read (their contents may be
+ *             anything, including NaN).
+ *   Causal    bottom-right aligned: key j is visible to query row i iff
+ *             j <= i + (L_b - sq); for sq == sk == L_b this is the usual
+ *             lower-triangular mask.  A row with no visible key gets O = 0
+ *             and LSE = -infinity.
+ *   Scale     must be finite and > 0 (typically 1/sqrt(head_dim)).
+ *   LSE units natural log of the sum of exp(scaled score).
+ *   Streams   work is enqueued on `stream` (NULL = legacy default stream);
+ *             the calls are asynchronous and never synchronise the device.
+ *   Errors    argument checks run on the host before anything is enqueued;
+ *             on any error nothing is launched.  No C++ exception crosses
+ *             this interface.  A kernel wait that exceeds its time limit
+ *             makes the kernel finish early and records FA_ERR_TIMEOUT in a
+ *             device error word, read by fa_get_device_error().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                    /* same type as cudaStream_t */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, hq % hkv != 0,
+                                 bad scale, decode with sq > FA_DECODE_MAX_SQ */
+    FA_ERR_UNSUPPORTED = 2,   /* head_dim not 64/96/128/256 (prefill) or not
+                                 64/128/256 (decode); device not sm_103 */
+    FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned */
+    FA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    FA_ERR_TIMEOUT = 5        /* a kernel wait ran out of time (device word) */
+} fa_status;
+
+/* Largest query count per sequence accepted by the decode entry points. */
+#define FA_DECODE_MAX_SQ 16
+
+/*
+ * Prefill forward.  Runs the warp-specialised tcgen05/TMEM kernel for
+ * head_dim in {64, 96, 128, 256}: a TMA producer warp streams K/V tiles
+ * through an mbarrier ring, one warp issues the score MMA (S = Q K^T) and the
+ * value MMA (O += P V) into tensor memory, softmax warpgroups turn S into P
+ * with exp2, and a correction/epilogue warpgroup rebases O and writes O and
+ * LSE ("b200-flash-attention4-planner", section A1 "Role example" and
+ * section E steps 3-8).
+ * Sizes: batch, hq, hkv, sq, sk >= 0 (any zero size is a no-op returning
+ * FA_OK, except sk == 0 with non-empty outputs, which writes O = 0 and
+ * LSE = -inf); batch <= 65535, hq <= 65535.
+ */
+fa_status fa_fwd_prefill(const void *q, const void *k, const void *v, void *o,
+                         float *lse, int batch, int hq, int hkv, int sq, int sk,
+                         const int *seqlens_k, int head_dim, float scale,
+                         int causal, fa_stream_t stream);
+
+/*
+ * Decode forward (few queries per sequence against a long key/value cache).
+ * Split-KV ("fa4-sm120-research" lists SplitKV among the features its kernels
+ * lack; "STAGE_D.md" gives the merge of attention over disjoint key sets by
+ * their LSE): each CTA handles one (batch entry, key/value head, key split),
+ * streams its keys with coalesced 16-byte loads, packs all query heads of the
+ * group onto the tensor-core M dimension and writes a partial (O_s, LSE_s);
+ * a second kernel combines the splits, weighting each by exp(LSE_s).  The
+ * merge is exact because the splits cover disjoint key sets.
+ * Same arguments as fa_fwd_prefill; sq must be 1..FA_DECODE_MAX_SQ and
+ * head_dim one of 64, 128, 256.  The partials live in a workspace that the
+ * call allocates and frees stream-ordered (cudaMallocAsync/cudaFreeAsync on
+ * `stream`).
+ */
+fa_status fa_fwd_decode(const void *q, const void *k, const void *v, void *o,
+                        float *lse, int batch, int hq, int hkv, int sq, int sk,
+                        const int *seqlens_k, int head_dim, float scale,
+                        int causal, fa_stream_t stream);
+
+/*
+ * fa_fwd_decode with an explicit number of key splits (num_splits <= 0 picks
+ * it automatically, exactly like fa_fwd_decode).  The splits partition
+ * [0, sk) into equal chunks of a multiple of 64 keys; any split count gives
+ * the same result up to rounding.
+ */
+fa_status fa_fwd_decode_splits(const void *q, const void *k, const void *v,
+                               void *o, float *lse, int batch, int hq, int hkv,
+                               int sq, int sk, const int *seqlens_k,
+                               int head_dim, float scale, int causal,
+                               int num_splits, fa_stream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *fa_status_string(fa_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns FA_ERR_TIMEOUT if any kernel recorded a wait time-out since
+ * the last call, FA_ERR_CUDA if synchronising failed, else FA_OK.
+ */
+fa_status fa_get_device_error(fa_stream_t stream);
+
+/*
+ * Like fa_get_device_error, and also stores the raw error word in *word_out
+ * (0 if none; FA time-outs are 0x1000 | site, where site numbers the wait
+ * that gave up).  word_out may be NULL.
+ */
+fa_status fa_get_device_error_word(fa_stream_t stream, unsigned int *word_out);
+
+/*
+ * Self-test of the time-out path: launches one block that waits on an
+ * mbarrier nobody arrives at, with a limit of `limit_ns` nanoseconds
+ * (clamped to [1e3, 1e9]).  The kernel gives up, records FA_ERR_TIMEOUT in
+ * the device error word and exits normally, so the context stays usable.
+ */
+fa_status fa_selftest_wait_timeout(long long limit_ns, fa_stream_t stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,96 @@
+"""The C-ABI library loads and exports every declared entry point; host-side
+argument validation rejects bad calls before any GPU work (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_blackwell_gb300 import binding, build
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("fa_fwd_prefill", "fa_fwd_decode", "fa_status_string",
+                     "fa_get_device_error", "fa_version"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from attention_forward_blackwell_gb300 import binding
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in binding.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    from attention_forward_blackwell_gb300 import binding
+    assert binding.status_string(0) == "FA_OK"
+    assert binding.status_string(5) == "FA_ERR_TIMEOUT"
+    assert binding.status_string(99) == "FA_ERR_UNKNOWN"
+    assert binding.version() >= 100
+
+
+P16 = ctypes.c_void_p(1 << 12)      # a 16-byte aligned (never dereferenced) address
+P_ODD = ctypes.c_void_p((1 << 12) + 8)
+
+
+@pytest.mark.parametrize("fn", ["fa_fwd_prefill", "fa_fwd_decode"])
+@pytest.mark.parametrize("args,expect", [
+    # (q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, seqlens, d, scale, causal), status
+    ((P16, P16, P16, P16, P16, -1, 1, 1, 1, 1, None, 64, 1.0, 0), 1),     # negative batch
+    ((P16, P16, P16, P16, P16, 1, 3, 2, 1, 1, None, 64, 1.0, 0), 1),      # hq % hkv
+    ((P16, P16, P16, P16, P16, 1, 1, 1, 1, 1, None, 64, 0.0, 0), 1),      # scale 0
+    ((P16, P16, P16, P16, P16, 1, 1, 1, 1, 1, None, 64, float("nan"), 0), 1),
+    ((None, P16, P16, P16, P16, 1, 1, 1, 1, 1, None, 64, 1.0, 0), 1),     # null q
+    ((P16, None, P16, P16, P16, 1, 1, 1, 1, 4, None, 64, 1.0, 0), 1),     # null k
+    ((P_ODD, P16, P16, P16, P16, 1, 1, 1, 1, 1, None, 64, 1.0, 0), 3),    # misaligned q
+    ((P16, P16, P16, P16, P16, 1, 1, 1, 1, 1, None, 80, 1.0, 0), 2),      # head_dim
+    ((P16, P16, P16, P16, P16, 70000, 1, 1, 1, 1, None, 64, 1.0, 0), 1),  # batch too big
+    ((None, None, None, None, None, 0, 4, 2, 8, 8, None, 64, 1.0, 0), 0),  # empty batch
+    ((None, None, None, None, None, 2, 4, 2, 0, 8, None, 64, 1.0, 1), 0),  # no queries
+])
+def test_host_validation(lib, fn, args, expect):
+    assert getattr(lib, fn)(*args, None) == expect
+
+
+def test_decode_specific_validation(lib):
+    # sq above the decode limit, and head_dim 96 (prefill only)
+    assert lib.fa_fwd_decode(P16, P16, P16, P16, P16, 1, 1, 1, 17, 8, None, 64, 1.0, 0,
+                             None) == 1
+    assert lib.fa_fwd_decode(P16, P16, P16, P16, P16, 1, 1, 1, 1, 8, None, 96, 1.0, 0,
+                             None) == 2
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    from attention_forward_blackwell_gb300 import binding
+    q = torch.zeros(1, 2, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        binding.prefill(q, q, q)          # CPU tensors: no fallback, refused
+    with pytest.raises(TypeError):
+        binding.prefill(q.float(), q, q)
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "attention_forward_blackwell_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text, f

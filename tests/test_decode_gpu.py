@@ -1,0 +1,100 @@
+"""Split-KV decode (split kernel + LSE combine) against the fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_parity import check_device_error, compare, free_cuda, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from attention_forward_blackwell_gb300 import build
+    build.build()
+    yield
+    free_cuda()
+
+
+def _decode(x, scale, causal=False, splits=0):
+    from attention_forward_blackwell_gb300 import binding
+    o, lse = binding.decode(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k,
+                            num_splits=splits)
+    torch.cuda.synchronize()
+    check_device_error()
+    return o, lse
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0, 1000])
+def test_split_counts_agree_with_oracle(splits):
+    """Any split count gives the oracle's result (merge over disjoint key sets)."""
+    from attention_forward_blackwell_gb300 import inputs
+    x = inputs.make_inputs(3, 8, 2, 1, 700, 128, tag=500, device="cuda", lengths=[700, 1, 333])
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    o, lse = _decode(x, 128 ** -0.5, splits=splits)
+    ro, rl = oracle_for(x, 128 ** -0.5, False)
+    compare(o, lse, ro, rl, f"decode splits={splits}")
+
+
+DECODE_SHAPES = [
+    # B, Hq, Hkv, Sq, Sk, d, causal, lengths
+    (2, 4, 4, 1, 513, 64, False, [513, 64]),
+    (2, 16, 1, 1, 900, 128, False, None),          # MQA, 16 heads on one tile
+    (1, 32, 2, 1, 400, 128, False, None),          # 16 heads per kv head
+    (2, 8, 2, 4, 600, 128, True, [600, 5]),        # 4 queries per sequence, causal
+    (1, 64, 2, 2, 300, 128, True, None),           # 64 rows per kv head -> 4 M tiles
+    (2, 8, 1, 1, 777, 256, False, [777, 300]),
+    (1, 4, 2, 16, 40, 64, True, None),             # more queries than keys for some rows
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,causal,lengths", DECODE_SHAPES)
+def test_decode_shapes(B, Hq, Hkv, Sq, Sk, d, causal, lengths):
+    from attention_forward_blackwell_gb300 import inputs
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=600 + Sk, device="cuda", lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    o, lse = _decode(x, 1 / math.sqrt(d), causal)
+    ro, rl = oracle_for(x, 1 / math.sqrt(d), causal)
+    compare(o, lse, ro, rl, f"decode {B,Hq,Hkv,Sq,Sk,d,causal}")
+
+
+def test_decode_matches_prefill_at_one_query():
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(2, 8, 2, 1, 1000, 128, tag=700, device="cuda")
+    od, ld = _decode(x, 0.088)
+    op, lp = binding.prefill(x.q, x.k, x.v, scale=0.088)
+    torch.cuda.synchronize()
+    assert (od.float() - op.float()).abs().max().item() <= 2e-2
+    assert (ld - lp).abs().max().item() <= 1e-3
+
+
+def test_empty_sequences():
+    from attention_forward_blackwell_gb300 import inputs
+    x = inputs.make_inputs(3, 4, 2, 1, 256, 128, tag=701, device="cuda", lengths=[0, 256, 0])
+    o, lse = _decode(x, 0.1)
+    assert torch.all(o[0] == 0) and torch.all(o[2] == 0)
+    assert torch.all(torch.isneginf(lse[0])) and torch.all(torch.isneginf(lse[2]))
+    ro, rl = oracle_for(x, 0.1, False)
+    compare(o, lse, ro, rl, "decode empty sequences")
+
+
+def test_full_decode_configuration_all_rows():
+    """The full decode workload (B=64, Hq=64, Hkv=8, d=128, L_b~U[1024,16384],
+    KV padded to 16384 with NaN past each length): every output row against
+    the oracle."""
+    from attention_forward_blackwell_gb300 import inputs, workloads
+    w = workloads.DECODE
+    x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device="cuda",
+                           lengths=w.lengths)
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    o, lse = _decode(x, w.scale)
+    ro, rl = oracle_for(x, w.scale, False)
+    compare(o, lse, ro, rl, "decode full config")
+    del x
+    free_cuda()
