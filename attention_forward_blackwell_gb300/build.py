@@ -7,6 +7,7 @@ when their source or any header is newer.
 from __future__ import annotations
 
 import os
+import platform
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
 
@@ -37,6 +38,11 @@ def _headers():
 
 def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -> str:
     os.makedirs(OBJDIR, exist_ok=True)
+    # objects from another host architecture (or toolchain) are never reused
+    stamp = os.path.join(OBJDIR, "host.txt")
+    host = f"{platform.machine()} {platform.system()}"
+    if not os.path.exists(stamp) or open(stamp).read() != host:
+        force = True
     nvcc = _nvcc()
     newest_header = max(os.path.getmtime(h) for h in _headers())
 
@@ -73,6 +79,8 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB_PATH)
+    with open(stamp, "w") as f:
+        f.write(host)
     return LIB_PATH
 
 
