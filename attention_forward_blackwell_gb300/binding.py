@@ -32,6 +32,8 @@ SIGNATURES = {
     "fa_get_device_error": (_I, [_VP]),
     "fa_get_device_error_word": (_I, [_VP, ctypes.POINTER(ctypes.c_uint)]),
     "fa_selftest_wait_timeout": (_I, [_LL, _VP]),
+    "fa_selftest_tmem_roundtrip": (_I, [_VP, _VP, _VP]),
+    "fa_selftest_mma_tile": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "fa_version": (_I, []),
 }
 
@@ -159,3 +161,26 @@ def get_device_error_word(stream=None):
 
 def selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return lib().fa_selftest_wait_timeout(int(limit_ns), _stream_ptr(stream))
+
+
+def selftest_tmem_roundtrip(x, stream=None):
+    """x: CUDA fp32 [128, 64]; returns the tensor-memory round trip of x."""
+    if x.dtype != torch.float32 or x.shape != (128, 64) or not x.is_cuda:
+        raise ValueError("x must be a CUDA fp32 tensor of shape [128, 64]")
+    x = x.contiguous()
+    out = torch.empty_like(x)
+    st = lib().fa_selftest_tmem_roundtrip(_ptr(x), _ptr(out), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_selftest_tmem_roundtrip")
+    return out
+
+
+def selftest_mma_tile(a, b, mode, stream=None):
+    """One 128x128 tile through the prefill kernel's MMA path (see fa.h)."""
+    a, b = a.contiguous(), b.contiguous()
+    d = torch.empty(128, 128, dtype=torch.float32, device=a.device)
+    st = lib().fa_selftest_mma_tile(_ptr(a), _ptr(b), _ptr(d), int(mode), int(a.shape[1]),
+                                    _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_selftest_mma_tile")
+    return d

@@ -293,6 +293,29 @@ fa_status fa_selftest_wait_timeout(long long limit_ns, fa_stream_t stream) {
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+fa_status fa_selftest_tmem_roundtrip(const float* in, float* out, fa_stream_t stream) {
+    if (!in || !out) return FA_ERR_INVALID_ARG;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    return from_cuda(launch_selftest_tmem_roundtrip(in, out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_selftest_mma_tile(const void* a, const void* b, float* d, int mode, int kdim,
+                               fa_stream_t stream) {
+    if (!a || !b || !d) return FA_ERR_INVALID_ARG;
+    if (mode == 1) kdim = 128;
+    if (mode != 0 && mode != 1) return FA_ERR_INVALID_ARG;
+    if (kdim != 64 && kdim != 128 && kdim != 256) return FA_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b)) return FA_ERR_MISALIGNED;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    return from_cuda(launch_selftest_mma_tile(static_cast<const uint16_t*>(a),
+                                              static_cast<const uint16_t*>(b), d, mode, kdim,
+                                              di->err_word, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fa_version(void) { return 100; }
 
 }  // extern "C"

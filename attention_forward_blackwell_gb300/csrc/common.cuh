@@ -71,6 +71,11 @@ cudaError_t launch_decode(const DecodeArgs& a, int head_dim, cudaStream_t s);
 cudaError_t launch_fill_empty(uint16_t* o, float* lse, long long rows, int head_dim,
                               cudaStream_t s);
 
+// Self-tests of the tcgen05 building blocks (selftest.cu).
+cudaError_t launch_selftest_tmem_roundtrip(const float* in, float* out, cudaStream_t s);
+cudaError_t launch_selftest_mma_tile(const uint16_t* a, const uint16_t* b, float* d, int mode,
+                                     int kdim, unsigned int* err_word, cudaStream_t s);
+
 // Self-test kernel for the bounded-wait path.
 cudaError_t launch_wait_timeout_selftest(unsigned int* err_word, unsigned long long limit_ns,
                                          cudaStream_t s);

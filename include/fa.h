@@ -139,6 +139,28 @@ fa_status fa_get_device_error_word(fa_stream_t stream, unsigned int *word_out);
  */
 fa_status fa_selftest_wait_timeout(long long limit_ns, fa_stream_t stream);
 
+/*
+ * Self-test of tensor memory: `in` and `out` are device fp32 [128 x 64].
+ * Row r is stored to tensor-memory lane r, loaded, multiplied by 1, stored,
+ * loaded again and written to `out`; the result must equal `in` bit for bit.
+ * (This is the "no-op round trip" that "STAGE_D.md" reports as corrupting
+ * data in its kernel; the prefill kernel's rebase and epilogue rely on it.)
+ */
+fa_status fa_selftest_tmem_roundtrip(const float *in, float *out, fa_stream_t stream);
+
+/*
+ * Self-test of one 128 x 128 output tile through the prefill kernel's
+ * shared-memory layout, descriptors and tcgen05.mma forms.  d: device fp32
+ * [128 x 128].
+ *   mode 0 (score MMA): a, b device bf16 [128 x kdim], kdim in {64, 128, 256};
+ *           d = a * b^T.
+ *   mode 1 (value MMA): a = P, b = V, both device bf16 [128 x 128]; P is placed
+ *           in tensor memory, V in shared memory (MN-major); d = a * b.
+ * Returns FA_ERR_INVALID_ARG for other modes or sizes.
+ */
+fa_status fa_selftest_mma_tile(const void *a, const void *b, float *d, int mode,
+                               int kdim, fa_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);
 
