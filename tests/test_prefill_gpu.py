@@ -85,16 +85,20 @@ def test_key_lengths_with_poisoned_padding(d, causal):
 
 
 def test_extreme_logits_one_hot_key():
-    """One key scores ~60 above the rest for every query; others are K*8."""
+    """K*8 gives scores with a spread of ~8.5 (max ~25 over 300 keys); key 17
+    is set to score 60.1 for every query (q_0 = 4, k_17 = (170, 0, ..., 0)),
+    so its weight is ~1 and every other weight is below e^-30."""
     from attention_forward_blackwell_gb300 import inputs
     d = 128
     x = inputs.make_inputs(1, 2, 2, 300, 300, d, tag=400, device="cuda", k_scale=8.0)
     x.q[..., 0] = 4.0
+    x.k[..., 17, :] = 0.0
     x.k[..., 17, 0] = 60.0 * math.sqrt(d) / 4.0
     o, lse = _run(x, 1.0 / math.sqrt(d), False)
     ro, rl = oracle_for(x, 1.0 / math.sqrt(d), False)
     compare(o, lse, ro, rl, "extreme logits")
-    assert float(lse.min()) > 40.0
+    assert float(lse.min()) > 55.0
+    assert (o.float() - x.v[:, :, 17:18].float()).abs().max().item() < 2e-2
 
 
 def test_zero_query_gives_mean_of_values():
