@@ -154,7 +154,7 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     int splits = num_splits;
     if (splits <= 0) {
         const long long pairs = (long long)batch * hkv * a.n_mtiles;
-        const long long target = 8ll * di->num_sms;    // CTAs worth keeping in flight
+        const long long target = 24ll * di->num_sms;   // CTAs worth keeping in flight
         long long want = (target + pairs - 1) / pairs;
         const long long max_splits = (sk + 255) / 256;  // at least 256 keys per split
         if (want > max_splits) want = max_splits;
