@@ -28,6 +28,7 @@ SIGNATURES = {
     "fa_fwd_prefill": (_I, _FWD + [_VP]),
     "fa_fwd_decode": (_I, _FWD + [_VP]),
     "fa_fwd_decode_splits": (_I, _FWD + [_I, _VP]),
+    "fa_fwd_decode_noalloc": (_I, _FWD + [_VP]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_get_device_error": (_I, [_VP]),
     "fa_get_device_error_word": (_I, [_VP, ctypes.POINTER(ctypes.c_uint)]),

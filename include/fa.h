@@ -114,6 +114,42 @@ fa_status fa_fwd_decode_splits(const void *q, const void *k, const void *v,
                                int head_dim, float scale, int causal,
                                int num_splits, fa_stream_t stream);
 
+/*
+ * Decode forward that allocates nothing (no counterpart in the source pages;
+ * it exists for users of this library).
+ *
+ * Who needs it: callers that cannot allocate device memory while they run --
+ * a serving loop that must not allocate once it is up (an allocation can
+ * stall or fail at an unpredictable moment), a process whose device memory
+ * is already held by another allocator so a new allocation would fail, or a
+ * deployment that must declare all of its device memory up front.
+ *
+ * Same arguments, layout and results as fa_fwd_decode.  Instead of a
+ * per-call workspace, the split partials live in one fixed device array of
+ * FA_DECODE_NOALLOC_SCRATCH_BYTES inside this library; every GPU that loads
+ * the library holds that array until the process exits.  A call needs
+ * n_splits * batch * hq * sq * (head_dim + 1) * 4 bytes of it; the call
+ * uses fewer key splits when needed to fit, and returns FA_ERR_INVALID_ARG
+ * when even one split does not fit (batch * hq * sq * (head_dim + 1) * 4 >
+ * FA_DECODE_NOALLOC_SCRATCH_BYTES).  The call itself makes no cudaMalloc,
+ * cudaFree or other allocating call.
+ *
+ * The first call on each device does a one-time set-up with that device
+ * current (it resolves the array's device address); make that first call
+ * before any stream capture.  All calls on a device share the one array and
+ * it keeps the last call's contents: nothing in it needs clearing (each call
+ * writes every partial it reads), but calls that overlap on the GPU -- on
+ * different streams, or from different host threads -- race on it and give
+ * wrong results.  Serialise them.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+fa_status fa_fwd_decode_noalloc(const void *q, const void *k, const void *v,
+                                void *o, float *lse, int batch, int hq, int hkv,
+                                int sq, int sk, const int *seqlens_k,
+                                int head_dim, float scale, int causal,
+                                fa_stream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *fa_status_string(fa_status status);
 
