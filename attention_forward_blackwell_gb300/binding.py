@@ -35,6 +35,8 @@ SIGNATURES = {
     "fa_selftest_wait_timeout": (_I, [_LL, _VP]),
     "fa_selftest_tmem_roundtrip": (_I, [_VP, _VP, _VP]),
     "fa_selftest_mma_tile": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
+    "fa_debug_prefill_trace": (_I, [_VP, _I]),
+    "fa_selftest_exp2_poly": (_I, [_VP, _VP, _I, _VP]),
     "fa_version": (_I, []),
 }
 
@@ -185,3 +187,25 @@ def selftest_mma_tile(a, b, mode, stream=None):
     if st != FA_OK:
         raise FaError(st, "fa_selftest_mma_tile")
     return d
+
+
+def debug_prefill_trace(buf=None, block=0):
+    """Install (or with buf=None remove) a prefill trace buffer: a CUDA
+    uint64/int64 tensor of at least 5 * 4096 elements (see fa.h)."""
+    if buf is not None and (buf.numel() < 5 * 4096 or buf.element_size() != 8 or not buf.is_cuda):
+        raise ValueError("trace buffer must be a CUDA 64-bit tensor of >= 20480 elements")
+    st = lib().fa_debug_prefill_trace(_ptr(buf), int(block))
+    if st != FA_OK:
+        raise FaError(st, "fa_debug_prefill_trace")
+
+
+def selftest_exp2_poly(x, stream=None):
+    """The prefill softmax's polynomial 2^x on a CUDA fp32 tensor."""
+    if x.dtype != torch.float32 or not x.is_cuda:
+        raise ValueError("x must be a CUDA fp32 tensor")
+    x = x.contiguous()
+    y = torch.empty_like(x)
+    st = lib().fa_selftest_exp2_poly(_ptr(x), _ptr(y), x.numel(), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_selftest_exp2_poly")
+    return y

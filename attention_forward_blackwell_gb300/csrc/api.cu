@@ -34,6 +34,10 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
+// Debug trace target of the next prefill launches (see fa_debug_prefill_trace).
+unsigned long long* g_trace_buf = nullptr;
+int g_trace_block = 0;
+
 // Looks up (once) the properties of the current device.  Returns nullptr if
 // the CUDA runtime fails.
 const DeviceInfo* device_info() {
@@ -220,6 +224,8 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     a.num_mblk = (sq + rows_per_cta - 1) / rows_per_cta;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_limit_ns = kWaitLimitNs;
+    a.trace = g_trace_buf;
+    a.trace_block = g_trace_block;
     p.head_dim = head_dim;
     p.causal = causal ? 1 : 0;
     cudaError_t e;
@@ -314,6 +320,21 @@ fa_status fa_selftest_mma_tile(const void* a, const void* b, float* d, int mode,
     return from_cuda(launch_selftest_mma_tile(static_cast<const uint16_t*>(a),
                                               static_cast<const uint16_t*>(b), d, mode, kdim,
                                               di->err_word, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_selftest_exp2_poly(const float* x, float* y, int n, fa_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !y))) return FA_ERR_INVALID_ARG;
+    const DeviceInfo* di = device_info();
+    if (!di) return FA_ERR_CUDA;
+    if (!di->supported) return FA_ERR_UNSUPPORTED;
+    return from_cuda(launch_selftest_exp2_poly(x, y, n, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+fa_status fa_debug_prefill_trace(unsigned long long* buf, int block) {
+    if (buf != nullptr && block < 0) return FA_ERR_INVALID_ARG;
+    g_trace_buf = buf;
+    g_trace_block = block;
+    return FA_OK;
 }
 
 int fa_version(void) { return 100; }

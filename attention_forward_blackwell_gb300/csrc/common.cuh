@@ -27,7 +27,17 @@ struct PrefillArgs {
     int num_mblk;               // CTAs along the query axis per (b, h)
     float scale_log2;           // scale * log2(e)
     unsigned long long wait_limit_ns;
+    // Debug trace (nullptr in normal use): one thread per role of CTA
+    // `trace_block` (linear block index) records SM clock stamps.
+    unsigned long long* trace;
+    int trace_block;
 };
+
+// Trace layout: kTraceSlots stamps per role; role r, event e of iteration j
+// lands at trace[r * kTraceSlots + j * kTraceEvents + e].
+constexpr int kTraceSlots = 4096;
+constexpr int kTraceEvents = 16;
+enum TraceRole { kTrMma = 0, kTrSoftmax0 = 1, kTrSoftmax1 = 2, kTrCorr = 3, kTrLoad = 4 };
 
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;   // 3-D maps {d, S, B*H}, box {64, 128, 1}
@@ -75,6 +85,8 @@ cudaError_t launch_fill_empty(uint16_t* o, float* lse, long long rows, int head_
 cudaError_t launch_selftest_tmem_roundtrip(const float* in, float* out, cudaStream_t s);
 cudaError_t launch_selftest_mma_tile(const uint16_t* a, const uint16_t* b, float* d, int mode,
                                      int kdim, unsigned int* err_word, cudaStream_t s);
+
+cudaError_t launch_selftest_exp2_poly(const float* x, float* y, int n, cudaStream_t s);
 
 // Self-test kernel for the bounded-wait path.
 cudaError_t launch_wait_timeout_selftest(unsigned int* err_word, unsigned long long limit_ns,

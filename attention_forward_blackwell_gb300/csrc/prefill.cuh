@@ -30,12 +30,12 @@
 //   NQ = 1: S buffers at [0, 128) and [128, 256), O at [256, 512).
 //
 // Hazard on the P/S alias: the next score MMA S_t(j+1) overwrites the upper
-// half of S_t, i.e. P_t(j), which the value MMA PV_t(j) reads.  The score MMA
-// is therefore issued in two N=64 halves: the lower half (which never holds
-// P) right after PV_t(j), the upper half only once PV_t(j) has completed
-// (tcgen05.commit -> mbarrier).  Distinct-accumulator MMAs are not ordered by
-// the ISA, so this wait is what makes the reuse safe; the lower-half MMA keeps
-// the tensor core busy while the MMA warp waits.
+// half of S_t, i.e. P_t(j), which the value MMA PV_t(j) reads.  MMAs with
+// different accumulators are not ordered by the ISA, so the MMA warp issues
+// S_t(j+1) only once PV_t(j) has completed (tcgen05.commit -> mbarrier); the
+// tensor core is busy with that PV while the warp waits.  Descriptors are
+// built once per CTA and advanced by address offsets, so each MMA issue is a
+// few integer adds and the instruction itself.
 //
 // Rebasing: the running max m is only moved when the block max exceeds it by
 // more than kRescaleThreshold (log2 units).  Until then P = exp2(s - m) may
@@ -51,6 +51,13 @@
 namespace fa {
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units (a factor of 256)
+// Optionally (kUsePolyExp2), in tiles without masked entries one pair of
+// exponentials in every kPolyEvery is computed by exp2_poly_x2 on the FMA
+// pipe instead of the MUFU ex2 instruction.  Measured on GB300 this is slower
+// at head_dim 128 (the softmax is bound by instruction issue, not by the MUFU
+// pipe), so it is off.
+constexpr bool kUsePolyExp2 = false;
+constexpr int kPolyEvery = 4;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -80,9 +87,9 @@ struct PrefillTraits {
     static constexpr uint32_t TMEM_COLS = 512;
     // Register split (threads x registers after setmaxnreg must not exceed
     // the launch allocation: 512 x 128 for NQ = 2, 384 x 168 for NQ = 1).
-    static constexpr uint32_t REG_SOFTMAX = (NQ == 2) ? 176 : 240;
-    static constexpr uint32_t REG_CORR = (NQ == 2) ? 80 : 88;
-    static constexpr uint32_t REG_OTHER = (NQ == 2) ? 80 : 80;
+    static constexpr uint32_t REG_SOFTMAX = (NQ == 2) ? 168 : 240;
+    static constexpr uint32_t REG_CORR = (NQ == 2) ? 88 : 88;
+    static constexpr uint32_t REG_OTHER = (NQ == 2) ? 88 : 80;
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 4096;
@@ -100,13 +107,13 @@ struct PrefillAux {
     uint64_t bar_full[T::NSLOT];
     uint64_t bar_empty[T::NSLOT];
     uint64_t bar_s_full[2];        // NQ = 2: per tile; NQ = 1: per score buffer
-    uint64_t bar_p_ready[T::NQ];
-    uint64_t bar_o_ready[T::NQ];
+    uint64_t bar_p_ready[T::NQ];   // P_t(j) written and O_t rebased (softmax + correction)
     uint64_t bar_pv_done[T::NQ];
     uint64_t bar_mb_full[T::NQ];
     uint64_t bar_mb_empty[T::NQ];
     uint64_t bar_epi[T::NQ];       // staging of O_t in shared memory complete
-    uint64_t bar_drain;
+    uint64_t bar_drain[2];
+    uint64_t bar_tail;             // producer-private: partial last value tile landed
     uint32_t tmem_base;
     int abort_flag;
     float mb_alpha[T::NQ][128];
@@ -116,10 +123,16 @@ struct PrefillAux {
 
 // Wait-site codes (recorded with kErrWaitTimeout on a time-out).
 enum : unsigned int {
-    kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteMmaO, kSiteMmaPv,
+    kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
     kSiteEpiStage
 };
+
+// Debug trace stamp (SM clock) by the calling thread, if tracing this CTA.
+__device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int j, int e) {
+    if (tr != nullptr && j * kTraceEvents + e < kTraceSlots)
+        tr[role * kTraceSlots + j * kTraceEvents + e] = (unsigned long long)clock64();
+}
 
 // Per-CTA work coordinates, computed identically by every thread.
 struct PrefillWork {
@@ -157,14 +170,33 @@ __device__ __forceinline__ uint32_t ring_slot(int p) { return (uint32_t)(p % T::
 template <class T>
 __device__ __forceinline__ uint32_t ring_phase(int p) { return (uint32_t)((p / T::NSLOT) & 1); }
 
+// Zeroes rows [rv, BN) of every 64-column chunk of one ring slot (all 32
+// lanes of the calling warp), then makes the writes visible to the tensor
+// core (async proxy).
+template <class T>
+__device__ __forceinline__ void zero_value_tail(uint32_t slot_addr, int rv) {
+    const int lane = threadIdx.x & 31;
+    const int granules = (T::BN - rv) * 8;   // 16-byte granules per chunk
+#pragma unroll
+    for (int c = 0; c < T::SLOT_CH; ++c) {
+        const uint32_t base = slot_addr + c * T::CHUNK + rv * 128;
+        for (int g = lane; g < granules; g += 32)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(base + g * 16), "r"(0)
+                         : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
 // ------------------------------------------------------------ producer ----
 
 template <class T>
 __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, const PrefillArgs& a,
                                   const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
-                                  uint32_t sRing, const WaitCtx& wc) {
+                                  uint32_t sRing, const WaitCtx& wc, unsigned long long* tr) {
     const int lane = threadIdx.x & 31;
+    if (lane != 0) tr = nullptr;
     if (w.n_max <= 0) return;
     const uint32_t bar_q = smem_u32(&aux->bar_q);
     if (lane == 0) {
@@ -189,8 +221,25 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         if (!mbar_wait(smem_u32(&aux->bar_empty[slot]), ring_phase<T>(p) ^ 1u, wc,
                        kErrWaitTimeout | kSiteLoadEmpty))
             break;
-        if (lane == 0) {
-            const uint32_t full = smem_u32(&aux->bar_full[slot]);
+        trace_mark(tr, kTrLoad, p >> 3, p & 7);
+        const uint32_t full = smem_u32(&aux->bar_full[slot]);
+        const int rv = w.L - j * T::BN;   // valid rows of this tile
+        if (kv == 1 && j == w.n_max - 1 && rv < T::BN) {
+            // Partial last value tile: rows [rv, BN) may hold anything (and a
+            // zero probability times a non-finite value would poison O), so
+            // they are zeroed before the tile is published to the MMA warps.
+            const uint32_t tail = smem_u32(&aux->bar_tail);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
+#pragma unroll
+                for (int c = 0; c < T::SLOT_CH; ++c)
+                    tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, tm_v,
+                                (pc * T::SLOT_CH + c) * 64, j * T::BN, w.b * a.Hkv + w.hk, tail);
+            }
+            if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail)) break;
+            zero_value_tail<T>(sRing + slot * T::SLOT, rv);
+            if (lane == 0) mbar_arrive(full);
+        } else if (lane == 0) {
             mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
             const CUtensorMap* m = kv ? tm_v : tm_k;
 #pragma unroll
@@ -215,61 +264,48 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 
 // ----------------------------------------------------------- MMA issue ----
 
-// Zeroes value rows [rv, BN) of a K/V tile held in ring slots starting at
-// position p (rows past the sequence length; they may hold anything, and a
-// zero probability times a non-finite value would poison O).
-template <class T>
-__device__ __forceinline__ void zero_value_tail(uint32_t sRing, int p, int rv) {
-    const int lane = threadIdx.x & 31;
-    const int granules = (T::BN - rv) * 8;   // 16-byte granules per chunk
-#pragma unroll
-    for (int pc = 0; pc < T::PIECES; ++pc) {
-        const uint32_t slot = ring_slot<T>(p + pc);
-#pragma unroll
-        for (int c = 0; c < T::SLOT_CH; ++c) {
-            const uint32_t base = sRing + slot * T::SLOT + c * T::CHUNK + rv * 128;
-            for (int g = lane; g < granules; g += 32)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(base + g * 16),
-                             "r"(0)
-                             : "memory");
-        }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
+// Descriptor address offset (bytes >> 4) of K-step kk inside a K-major
+// operand stored as 64-column chunks of 128 rows: chunk kk/4, then 32 bytes
+// per step inside the 128-byte swizzled row.
+__device__ __forceinline__ constexpr uint64_t kstep_off(int kk) {
+    return (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4);
 }
 
-// Score MMA S[cols] = Q_t * K^T over all head dims, for K rows [64 hf, 64 hf + n).
+// Score MMA S[128 x 128] = Q_t K_j^T: one N = 128 instruction per K-step of
+// 16 head dims.  qd: descriptor of the Q tile; kd[p]: descriptors of the ring
+// slots that hold the K tile (two slots for head_dim 256).
 template <class T>
-__device__ __forceinline__ void issue_score(uint32_t tmem_d, uint32_t sQt, uint32_t sRing,
-                                            int posK, int hf, uint32_t idesc) {
+__device__ __forceinline__ void issue_score(uint32_t tmem_d, uint64_t qd,
+                                            const uint64_t (&kd)[T::PIECES], uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < T::KSTEPS; ++kk) {
         const int piece = kk / (T::SLOT_CH * 4);
-        const int ch = (kk / 4) % T::SLOT_CH;
-        const uint32_t a_addr = sQt + (kk / 4) * T::CHUNK + (kk % 4) * 32;
-        const uint32_t b_addr = sRing + ring_slot<T>(posK + piece) * T::SLOT + ch * T::CHUNK +
-                                hf * 64 * 128 + (kk % 4) * 32;
-        umma_ss(tmem_d, sdesc_sw128(a_addr, 16, 1024), sdesc_sw128(b_addr, 16, 1024), idesc,
-                kk > 0 ? 1u : 0u);
+        const int kin = kk % (T::SLOT_CH * 4);
+        umma_ss(tmem_d, qd + kstep_off(kk), kd[piece] + kstep_off(kin), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-// Value MMA O[:, n-half] (+)= P * V over 128 keys (8 steps of 16 keys).
+// Value MMA O[:, 0:N] (+)= P V over 128 keys: 8 steps of 16 keys.  V is
+// MN-major: 16 keys are two 8-row swizzle atoms, 2048 bytes per step.
 template <class T>
-__device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_slot_addr,
+__device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, uint64_t vd,
                                             uint32_t idesc, bool first) {
 #pragma unroll
-    for (int kk = 0; kk < T::BN / 16; ++kk) {
-        const uint64_t bd = sdesc_sw128(v_slot_addr + kk * 2048, T::CHUNK, 1024);
-        umma_ts(tmem_o, tmem_p + kk * 8, bd, idesc, (!first || kk > 0) ? 1u : 0u);
-    }
+    for (int kk = 0; kk < T::BN / 16; ++kk)
+        umma_ts(tmem_o, tmem_p + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc,
+                (!first || kk > 0) ? 1u : 0u);
 }
 
+// MMA issue: one elected lane of one warp issues every tcgen05.mma of the CTA
+// and the commits that release K/V slots and signal the softmax/correction
+// warpgroups.
 template <class T>
-__device__ void prefill_mma_role(const PrefillArgs& a, const PrefillWork& w, PrefillAux<T>* aux,
-                                 uint32_t tmem, uint32_t sQ, uint32_t sRing, const WaitCtx& wc) {
+__device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork& w,
+                                 PrefillAux<T>* aux, uint32_t tmem, uint32_t sQ, uint32_t sRing,
+                                 const WaitCtx& wc, unsigned long long* tr) {
     const int lane = threadIdx.x & 31;
     const bool leader = lane == 0;
+    if (!leader || tq != 0) tr = nullptr;
     auto full_bar = [&](int p) { return smem_u32(&aux->bar_full[ring_slot<T>(p)]); };
     auto empty_bar = [&](int p) { return smem_u32(&aux->bar_empty[ring_slot<T>(p)]); };
     auto wait_tile = [&](int p0, unsigned site) {
@@ -278,134 +314,154 @@ __device__ void prefill_mma_role(const PrefillArgs& a, const PrefillWork& w, Pre
                 return false;
         return true;
     };
-    auto release_tile = [&](int p0) {
+    // release a K or V tile once the MMAs issued so far (which read it) complete
+    auto release_tile = [&](int p0, bool) {
         if (leader)
             for (int pc = 0; pc < T::PIECES; ++pc) tc_commit(empty_bar(p0 + pc));
     };
+    // descriptors of the Q tiles and of ring slot 0, built once; everything
+    // else is an address offset added to them
+    const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);            // K-major Q
+    const uint64_t kd0 = sdesc_sw128(sRing, 16, 1024);         // K-major K
+    const uint64_t vd0 = sdesc_sw128(sRing, T::CHUNK, 1024);   // MN-major V
+    auto qdesc = [&](int t) { return qd0 + (uint64_t)((t * T::QTILE) >> 4); };
+    auto slot_off = [&](int p) { return (uint64_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
+    auto kdesc = [&](int p0, uint64_t (&kd)[T::PIECES]) {
+#pragma unroll
+        for (int pc = 0; pc < T::PIECES; ++pc) kd[pc] = kd0 + slot_off(p0 + pc);
+    };
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
+    uint64_t kd[T::PIECES];
 
     if (w.n_max > 0) do {
         if (!mbar_wait(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
-        if (!wait_tile(0, kSiteMmaK)) break;
-        tc_fence_after();
-        bool ok = true;
         if constexpr (T::NQ == 2) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, 64, false, false);
-            constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
+            // one issuing warp alternates the tiles: PV_0(j), S_0(j+1),
+            // PV_1(j), S_1(j+1); each softmax overlaps the other tile's MMAs
+            if (!wait_tile(0, kSiteMmaK)) break;
+            tc_fence_after();
+            kdesc(0, kd);
             if (leader) {
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (w.n_kv[t] <= 0) continue;
-                    issue_score<T>(tmem + T::s_col(t), sQ + t * T::QTILE, sRing, 0, 0, idesc_s);
-                    issue_score<T>(tmem + T::s_col(t) + 64, sQ + t * T::QTILE, sRing, 0, 1, idesc_s);
+                    issue_score<T>(tmem + T::s_col(t), qdesc(t), kd, idesc_s);
                     tc_commit(smem_u32(&aux->bar_s_full[t]));
                 }
             }
-            release_tile(0);
+            release_tile(0, false);
             __syncwarp();
+            bool ok = true;
             for (int j = 0; j < w.n_max && ok; ++j) {
                 const int posV = (2 * j + 1) * T::PIECES;
                 const int posK = (2 * j + 2) * T::PIECES;
-                if (!wait_tile(posV, kSiteMmaV)) { ok = false; break; }
-                if (j == w.n_max - 1 && w.L - j * T::BN < T::BN)
-                    zero_value_tail<T>(sRing, posV, w.L - j * T::BN);
+                const uint32_t ph = (uint32_t)(j & 1);
+                if (!wait_tile(posV, kSiteMmaV)) break;
+                trace_mark(tr, kTrMma, j, 0);
                 bool k_next_ready = false;
+#pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j >= w.n_kv[t]) continue;
-                    const uint32_t ph = (uint32_t)(j & 1);
-                    if (!mbar_wait(smem_u32(&aux->bar_p_ready[t]), ph, wc, kErrWaitTimeout | kSiteMmaP) ||
-                        !mbar_wait(smem_u32(&aux->bar_o_ready[t]), ph, wc, kErrWaitTimeout | kSiteMmaO)) {
+                    if (!mbar_wait(smem_u32(&aux->bar_p_ready[t]), ph, wc,
+                                   kErrWaitTimeout | kSiteMmaP)) {
                         ok = false;
                         break;
                     }
+                    trace_mark(tr, kTrMma, j, 1 + 3 * t);
                     tc_fence_after();
                     if (leader) {
                         issue_value<T>(tmem + T::o_col(t), tmem + T::s_col(t) + 64,
-                                       sRing + ring_slot<T>(posV) * T::SLOT, idesc_v, j == 0);
+                                       vd0 + slot_off(posV), idesc_v, j == 0);
                         tc_commit(smem_u32(&aux->bar_pv_done[t]));
-                        if (t == 1) tc_commit(empty_bar(posV));   // V_j fully consumed
                     }
+                    if (t == 1) release_tile(posV, false);   // V_j fully consumed
+                    trace_mark(tr, kTrMma, j, 2 + 3 * t);
                     __syncwarp();
                     if (j + 1 < w.n_kv[t]) {
                         if (!k_next_ready) {
                             if (!wait_tile(posK, kSiteMmaK)) { ok = false; break; }
                             k_next_ready = true;
-                            tc_fence_after();
+                            trace_mark(tr, kTrMma, j, 7);
+                            kdesc(posK, kd);
                         }
-                        if (leader)
-                            issue_score<T>(tmem + T::s_col(t), sQ + t * T::QTILE, sRing, posK, 0,
-                                           idesc_s);
-                        __syncwarp();
-                        // the upper half overwrites P_t(j): wait until PV_t(j) is done
+                        // S_t(j+1) overwrites P_t(j): PV_t(j) must have completed
                         if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), ph, wc,
                                        kErrWaitTimeout | kSiteMmaPv)) {
                             ok = false;
                             break;
                         }
+                        trace_mark(tr, kTrMma, j, 3 + 3 * t);
                         tc_fence_after();
                         if (leader) {
-                            issue_score<T>(tmem + T::s_col(t) + 64, sQ + t * T::QTILE, sRing, posK,
-                                           1, idesc_s);
+                            issue_score<T>(tmem + T::s_col(t), qdesc(t), kd, idesc_s);
                             tc_commit(smem_u32(&aux->bar_s_full[t]));
                         }
+                        trace_mark(tr, kTrMma, j, 9 + t);
                         __syncwarp();
                     }
                 }
-                if (ok && j + 1 < w.n_max) release_tile(posK);
+                if (ok && j + 1 < w.n_max) release_tile(posK, false);
+                trace_mark(tr, kTrMma, j, 8);
                 __syncwarp();
             }
         } else {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
-            constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
+            if (!wait_tile(0, kSiteMmaK)) break;
+            tc_fence_after();
+            kdesc(0, kd);
             if (leader) {
-                issue_score<T>(tmem + T::s_col(0), sQ, sRing, 0, 0, idesc_s);
+                issue_score<T>(tmem + T::s_col(0), qdesc(0), kd, idesc_s);
                 tc_commit(smem_u32(&aux->bar_s_full[0]));
             }
-            release_tile(0);
+            release_tile(0, false);
             __syncwarp();
             for (int j = 0; j < w.n_max; ++j) {
                 const int posV = (2 * j + 1) * T::PIECES;
                 const int posK = (2 * j + 2) * T::PIECES;
+                // next score first, into the other buffer; that buffer held
+                // P(j-1), so PV(j-1) must have completed
                 if (j + 1 < w.n_max) {
-                    if (!wait_tile(posK, kSiteMmaK)) { ok = false; break; }
-                    // buffer (j+1)%2 held P(j-1): PV(j-1) must have completed
-                    if (j >= 1 && !mbar_wait(smem_u32(&aux->bar_pv_done[0]), (uint32_t)((j - 1) & 1),
-                                             wc, kErrWaitTimeout | kSiteMmaPv)) {
-                        ok = false;
+                    if (!wait_tile(posK, kSiteMmaK)) break;
+                    if (j >= 1 && !mbar_wait(smem_u32(&aux->bar_pv_done[0]),
+                                             (uint32_t)((j - 1) & 1), wc,
+                                             kErrWaitTimeout | kSiteMmaPv))
                         break;
-                    }
                     tc_fence_after();
+                    kdesc(posK, kd);
                     if (leader) {
-                        issue_score<T>(tmem + T::s_col((j + 1) & 1), sQ, sRing, posK, 0, idesc_s);
+                        issue_score<T>(tmem + T::s_col((j + 1) & 1), qdesc(0), kd, idesc_s);
                         tc_commit(smem_u32(&aux->bar_s_full[(j + 1) & 1]));
                     }
-                    release_tile(posK);
+                    release_tile(posK, false);
                     __syncwarp();
                 }
-                if (!wait_tile(posV, kSiteMmaV)) { ok = false; break; }
-                if (j == w.n_max - 1 && w.L - j * T::BN < T::BN)
-                    zero_value_tail<T>(sRing, posV, w.L - j * T::BN);
-                const uint32_t ph = (uint32_t)(j & 1);
-                if (!mbar_wait(smem_u32(&aux->bar_p_ready[0]), ph, wc, kErrWaitTimeout | kSiteMmaP) ||
-                    !mbar_wait(smem_u32(&aux->bar_o_ready[0]), ph, wc, kErrWaitTimeout | kSiteMmaO)) {
-                    ok = false;
+                if (!wait_tile(posV, kSiteMmaV)) break;
+                trace_mark(tr, kTrMma, j, 0);
+                if (!mbar_wait(smem_u32(&aux->bar_p_ready[0]), (uint32_t)(j & 1), wc,
+                               kErrWaitTimeout | kSiteMmaP))
                     break;
-                }
+                trace_mark(tr, kTrMma, j, 1);
                 tc_fence_after();
                 if (leader) {
 #pragma unroll
                     for (int nh = 0; nh < T::PIECES; ++nh)
-                        issue_value<T>(tmem + T::o_col(0) + nh * 128, tmem + T::s_col(j & 1) + 64,
-                                       sRing + ring_slot<T>(posV + nh) * T::SLOT, idesc_v, j == 0);
+                        issue_value<T>(tmem + T::o_col(0) + nh * 128,
+                                       tmem + T::s_col(j & 1) + 64, vd0 + slot_off(posV + nh),
+                                       idesc_v, j == 0);
                     tc_commit(smem_u32(&aux->bar_pv_done[0]));
                 }
-                release_tile(posV);
+                release_tile(posV, false);
+                trace_mark(tr, kTrMma, j, 2);
                 __syncwarp();
             }
         }
     } while (0);
-    // All MMAs of this CTA must have completed before tensor memory is freed.
+    // All MMAs issued by this warp must have completed before tensor memory
+    // is freed.
     if (leader) {
-        tc_commit(smem_u32(&aux->bar_drain));
-        mbar_wait_drain(smem_u32(&aux->bar_drain), 0, a.wait_limit_ns);
+        const uint32_t drain = smem_u32(&aux->bar_drain[tq]);
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0, a.wait_limit_ns);
     }
     __syncwarp();
 }
@@ -414,8 +470,11 @@ __device__ void prefill_mma_role(const PrefillArgs& a, const PrefillWork& w, Pre
 
 template <class T, bool CAUSAL>
 __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillWork& w,
-                                     PrefillAux<T>* aux, uint32_t tmem, const WaitCtx& wc) {
+                                     PrefillAux<T>* aux, uint32_t tmem, const WaitCtx& wc,
+                                     unsigned long long* tr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if ((warp & 3) != 0 || lane != 0) tr = nullptr;
+    const int trole = t == 0 ? kTrSoftmax0 : kTrSoftmax1;
     const int r = (warp & 3) * 32 + lane;                    // tile row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int row = w.row0 + t * T::BM + r;
@@ -431,28 +490,44 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
     for (int j = 0; j < nk; ++j) {
         const int sb = (T::NSBUF == 2) ? (j & 1) : 0;
         const uint32_t scol = (T::NQ == 2) ? T::s_col(t) : T::s_col(sb);
-        const uint32_t bar_s = smem_u32(&aux->bar_s_full[(T::NQ == 2) ? t : sb]);
-        const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
-        if (!mbar_wait(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) { ok = false; break; }
-        tc_fence_after();
         uint32_t u[4][32];
+        {
+            const uint32_t bar_s = smem_u32(&aux->bar_s_full[(T::NQ == 2) ? t : sb]);
+            const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+            if (!mbar_wait(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
+                ok = false;
+                break;
+            }
+            trace_mark(tr, trole, j, 0);
+            trace_mark(tr, trole, j, 1);
+            tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + scol + q * 32, u[q]);
+            for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + scol + q * 32, u[q]);
+        }
         tmem_wait_ld();
+        trace_mark(tr, trole, j, 2);
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
         // mask: only tiles that reach past this row's last visible key
         const int kv0 = j * T::BN;
-        if (lim - kv0 < T::BN - 1) {
+        const bool masked = lim - kv0 < T::BN - 1;
+        const bool warp_masked = __any_sync(0xffffffffu, masked);
+        if (masked) {
             const int nvis = lim - kv0 + 1;                  // visible columns (may be <= 0)
 #pragma unroll
             for (int c = 0; c < 128; ++c) s[c] = (c < nvis) ? s[c] : -INFINITY;
         }
-        float mx = fmax3(s[0], s[1], s[2]);
+        // row max: four independent 3-input-max chains, then combine
+        float mq[4];
 #pragma unroll
-        for (int c = 3; c < 127; c += 2) mx = fmax3(mx, s[c], s[c + 1]);
-        mx = fmaxf(mx, s[127]);
+        for (int q = 0; q < 4; ++q) {
+            float m = fmax3(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+            for (int c = 3; c < 31; c += 2) m = fmax3(m, s[32 * q + c], s[32 * q + c + 1]);
+            mq[q] = fmaxf(m, s[32 * q + 31]);
+        }
+        const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
         const float m_new = fmaxf(m_run, mx * sl2);
         float alpha = 1.f;
         if (m_new > m_run + kRescaleThreshold) {
@@ -465,30 +540,50 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
             break;
         }
         aux->mb_alpha[t][r] = alpha;
-        mbar_arrive(mb_full);
+        mbar_arrive_warp(mb_full);
+        trace_mark(tr, trole, j, 3);
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
-        float rs0 = 0.f, rs1 = 0.f;
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 nbase = make_float2(-base, -base);
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
         uint32_t pk[2][32];
+        if (warp_masked) {
+            // masked entries are -inf and must give exactly 0: hardware ex2 only
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-            const float p0 = ex2_approx(fmaf(s[2 * c], sl2, -base));
-            const float p1 = ex2_approx(fmaf(s[2 * c + 1], sl2, -base));
-            rs0 += p0;
-            rs1 += p1;
-            pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+            for (int c = 0; c < 64; ++c) {
+                const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, nbase);
+                const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rs[c & 3] = fadd2(rs[c & 3], p);
+                pk[c >> 5][c & 31] = pack_bf16x2(p.x, p.y);
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, nbase);
+                const float2 p = (kUsePolyExp2 && c % kPolyEvery == kPolyEvery - 1)
+                                     ? exp2_poly_x2(x)
+                                     : make_float2(ex2_approx(x.x), ex2_approx(x.y));
+                rs[c & 3] = fadd2(rs[c & 3], p);
+                pk[c >> 5][c & 31] = pack_bf16x2(p.x, p.y);
+            }
         }
-        l_run = fmaf(l_run, alpha, rs0 + rs1);
+        const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
+        const float2 rsum = fadd2(rs01, rs23);
+        l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
+        trace_mark(tr, trole, j, 4);
         tmem_st32(lane_base + scol + 64, pk[0]);
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(smem_u32(&aux->bar_p_ready[t]));
+        mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));
+        trace_mark(tr, trole, j, 5);
     }
     if (ok) {   // final message nk: row statistics for the epilogue
         if (mbar_wait(mb_empty, (uint32_t)((nk & 1) ^ 1), wc, kErrWaitTimeout | kSiteSmMbox)) {
             aux->mb_l[t][r] = l_run;
             aux->mb_m[t][r] = m_run;
-            mbar_arrive(mb_full);
+            mbar_arrive_warp(mb_full);
         }
     }
 }
@@ -498,8 +593,9 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
 template <class T>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
                                         const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
-                                        uint32_t sQ, const WaitCtx& wc) {
+                                        uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if ((warp & 3) != 0 || lane != 0) tr = nullptr;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const bool issuer = (warp & 3) == 0 && lane == 0;
@@ -512,8 +608,9 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 ok = false;
                 break;
             }
+            trace_mark(tr, kTrCorr, j, 4 * t);
             const float alpha = aux->mb_alpha[t][r];
-            mbar_arrive(smem_u32(&aux->bar_mb_empty[t]));
+            mbar_arrive_warp(smem_u32(&aux->bar_mb_empty[t]));
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
                 if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((j - 1) & 1), wc,
@@ -534,7 +631,8 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive(smem_u32(&aux->bar_o_ready[t]));
+            mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));   // O_t safe for PV_t(j)
+            trace_mark(tr, kTrCorr, j, 4 * t + 1);
         }
     }
     // epilogue: O / row_sum -> bf16 -> shared (Q tile's space, 128-byte swizzled) -> TMA store
@@ -545,6 +643,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             ok = false;
             break;
         }
+        trace_mark(tr, kTrCorr, w.n_max, 4 * t);
         const float l = aux->mb_l[t][r];
         const float m = aux->mb_m[t][r];
         if (nk > 0) {
@@ -589,7 +688,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] = lse;
         }
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&aux->bar_epi[t]));
+        mbar_arrive_warp(smem_u32(&aux->bar_epi[t]));
         if (issuer && w.row0 + t * T::BM < a.Sq &&
             mbar_wait_lane(smem_u32(&aux->bar_epi[t]), 0, wc, kErrWaitTimeout | kSiteEpiStage)) {
 #pragma unroll
@@ -598,6 +697,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                              w.b * a.Hq + w.h);
             bulk_commit_group();
         }
+        trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
     }
     if (issuer) bulk_wait_group_0();
 }
@@ -627,15 +727,17 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             mbar_init(smem_u32(&aux->bar_empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&aux->bar_s_full[i]), 1);
+        // warpgroup-to-warp signals: one elected arrive per warp
         for (int t = 0; t < T::NQ; ++t) {
-            mbar_init(smem_u32(&aux->bar_p_ready[t]), 128);
-            mbar_init(smem_u32(&aux->bar_o_ready[t]), 128);
+            mbar_init(smem_u32(&aux->bar_p_ready[t]), 8);   // 4 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_pv_done[t]), 1);
-            mbar_init(smem_u32(&aux->bar_mb_full[t]), 128);
-            mbar_init(smem_u32(&aux->bar_mb_empty[t]), 128);
-            mbar_init(smem_u32(&aux->bar_epi[t]), 128);
+            mbar_init(smem_u32(&aux->bar_mb_full[t]), 4);
+            mbar_init(smem_u32(&aux->bar_mb_empty[t]), 4);
+            mbar_init(smem_u32(&aux->bar_epi[t]), 4);
         }
-        mbar_init(smem_u32(&aux->bar_drain), 1);
+        mbar_init(smem_u32(&aux->bar_drain[0]), 1);
+        mbar_init(smem_u32(&aux->bar_drain[1]), 1);
+        mbar_init(smem_u32(&aux->bar_tail), 1);
         aux->abort_flag = 0;
         mbar_fence_init();
     }
@@ -648,19 +750,22 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = aux->tmem_base;
     const WaitCtx wc{&aux->abort_flag, args.err_word, args.wait_limit_ns};
+    const int block_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    unsigned long long* tr = (args.trace != nullptr && block_lin == args.trace_block) ? args.trace
+                                                                                     : nullptr;
 
     if (wg < T::NQ) {
         setmaxnreg_inc<T::REG_SOFTMAX>();
-        prefill_softmax_role<T, CAUSAL>(wg, args, w, aux, tmem, wc);
+        prefill_softmax_role<T, CAUSAL>(wg, args, w, aux, tmem, wc, tr);
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::REG_CORR>();
-        prefill_correction_role<T>(&tm_o, args, w, aux, tmem, sQ, wc);
+        prefill_correction_role<T>(&tm_o, args, w, aux, tmem, sQ, wc, tr);
     } else {
         setmaxnreg_dec<T::REG_OTHER>();
         if (warp == T::MMA_WARP)
-            prefill_mma_role<T>(args, w, aux, tmem, sQ, sRing, wc);
+            prefill_mma_role<T>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
         else if (warp == T::LOAD_WARP)
-            prefill_load_role<T>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc);
+            prefill_load_role<T>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc, tr);
     }
 
     tc_fence_before();

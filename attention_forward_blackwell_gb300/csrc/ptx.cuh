@@ -50,6 +50,13 @@ __device__ __forceinline__ void mbar_fence_init() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
+// One arrive on behalf of the whole warp, after every lane's prior work
+// (the __syncwarp orders the lanes' memory operations before lane 0's
+// release-arrive).
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
@@ -277,6 +284,53 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Packed fp32 pair arithmetic (two lanes of work per instruction).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// 2^x for a pair of floats on the FMA/ALU pipes instead of the MUFU (XU)
+// pipe.  Method: range reduction n = round(x) by adding and subtracting
+// 1.5 * 2^23 (the fraction bits of the sum then hold n), f = x - n in
+// [-1/2, 1/2]; 2^f from a cubic fitted by a Remez exchange for minimax
+// relative error on [-1/2, 1/2] (max relative error 7.5e-5); the result's
+// exponent is n added into the IEEE-754 exponent field by integer addition.
+// Inputs are clamped at -125 so the exponent arithmetic can neither wrap nor
+// reach the denormal encoding; results for x < -125 are therefore about
+// 2^-125 (tiny, never exactly zero), so callers use it only where no entry is
+// masked.
+__device__ __forceinline__ float2 exp2_poly_x2(float2 x) {
+    constexpr float kMagic = 12582912.0f;   // 1.5 * 2^23
+    constexpr float c0 = 0.99992805719375610f, c1 = 0.69326096773147583f;
+    constexpr float c2 = 0.24261112511157990f, c3 = 0.05517166852951050f;
+    x.x = fmaxf(x.x, -125.0f);
+    x.y = fmaxf(x.y, -125.0f);
+    const float2 t = fadd2(x, make_float2(kMagic, kMagic));                // n in low bits
+    const float2 n = fadd2(t, make_float2(-kMagic, -kMagic));              // round(x)
+    const float2 f = ffma2(n, make_float2(-1.0f, -1.0f), x);               // x - n
+    float2 q = ffma2(f, make_float2(c3, c3), make_float2(c2, c2));
+    q = ffma2(q, f, make_float2(c1, c1));
+    q = ffma2(q, f, make_float2(c0, c0));
+    // (bits(t) << 23) == n << 23 modulo 2^32, because bits(1.5 * 2^23) << 23
+    // vanishes modulo 2^32
+    return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+                       __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

@@ -157,7 +157,25 @@ __global__ void __launch_bounds__(128) mma_tile_kernel(const uint16_t* a, const 
     }
 }
 
+__global__ void exp2_poly_kernel(const float* x, float* y, int n) {
+    const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+    if (i + 1 < n) {
+        const float2 r = exp2_poly_x2(make_float2(x[i], x[i + 1]));
+        y[i] = r.x;
+        y[i + 1] = r.y;
+    } else if (i < n) {
+        y[i] = exp2_poly_x2(make_float2(x[i], 0.f)).x;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_exp2_poly(const float* x, float* y, int n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    const int threads = 256, pairs = (n + 1) / 2;
+    exp2_poly_kernel<<<(pairs + threads - 1) / threads, threads, 0, s>>>(x, y, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_selftest_tmem_roundtrip(const float* in, float* out, cudaStream_t s) {
     tmem_roundtrip_kernel<<<1, 128, 0, s>>>(in, out);

@@ -197,6 +197,26 @@ fa_status fa_selftest_tmem_roundtrip(const float *in, float *out, fa_stream_t st
 fa_status fa_selftest_mma_tile(const void *a, const void *b, float *d, int mode,
                                int kdim, fa_stream_t stream);
 
+/*
+ * Self-test of the polynomial exp2 that the prefill softmax uses for part of
+ * its exponentials (x, y: device fp32 [n]); y[i] approximates 2^x[i] with a
+ * relative error below 1e-4 for x in [-125, 126]; inputs below -125 are
+ * clamped, giving about 2^-125.  Tested against the exact 2^x.
+ */
+fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t stream);
+
+/*
+ * Debug tracing of the prefill kernel (not for production use; not
+ * thread-safe).  With `buf` a device buffer of at least 5 * 4096 uint64
+ * values, the following prefill launches make one thread of each role of the
+ * CTA with linear index `block` (x + gridDim.x * (y + gridDim.y * z)) record
+ * SM clock stamps at its pipeline events: role r (0 MMA issue, 1 and 2
+ * softmax of query tile 0 and 1, 3 correction/epilogue, 4 TMA producer),
+ * event e of key/value iteration j at buf[r * 4096 + j * 16 + e].  Unused
+ * slots are left untouched.  buf = NULL switches tracing off.
+ */
+fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);
 

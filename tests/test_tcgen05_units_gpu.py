@@ -46,3 +46,21 @@ def test_value_mma_tile():
     err = (d.double() - ref).abs().max().item()
     print("value tile max err", err)
     assert err < 1e-2
+
+
+def test_polynomial_exp2_against_exact():
+    """The FMA-pipe exp2 used for part of the softmax: relative error below
+    1e-4 against the exact 2^x wherever the result is a normal float
+    (x in [-125, 126]), and tiny positive normal values further down (inputs
+    are clamped at -125)."""
+    import numpy as np
+    from attention_forward_blackwell_gb300 import binding
+    xs = np.concatenate([np.linspace(-125, 126, 400001), np.arange(-125, 127, 1.0),
+                         np.arange(-125, 126, 1.0) + 0.5]).astype(np.float32)
+    y = binding.selftest_exp2_poly(torch.from_numpy(xs).cuda()).cpu().numpy().astype(np.float64)
+    rel = np.abs(y / np.exp2(xs.astype(np.float64)) - 1)
+    print("poly exp2 max rel err", rel.max())
+    assert rel.max() < 1e-4
+    low = binding.selftest_exp2_poly(torch.tensor([-126.0, -127.0, -500.0, -float("inf")],
+                                                  device="cuda")).cpu().numpy()
+    assert np.all(low > 0) and np.all(low < 2.0 ** -124)
