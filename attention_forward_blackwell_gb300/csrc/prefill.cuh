@@ -110,7 +110,6 @@ struct PrefillAux {
     uint64_t bar_p_ready[T::NQ];   // P_t(j) written and O_t rebased (softmax + correction)
     uint64_t bar_pv_done[T::NQ];
     uint64_t bar_mb_full[T::NQ];
-    uint64_t bar_mb_empty[T::NQ];
     uint64_t bar_epi[T::NQ];       // staging of O_t in shared memory complete
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
@@ -303,14 +302,21 @@ template <class T>
 __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork& w,
                                  PrefillAux<T>* aux, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                                  const WaitCtx& wc, unsigned long long* tr) {
+    // The whole role runs on lane 0: tcgen05.mma and tcgen05.commit are
+    // issued by a single thread, and lane-level waits avoid warp collectives
+    // on the issue path.  Lanes 1..31 wait at the final __syncwarp.
     const int lane = threadIdx.x & 31;
-    const bool leader = lane == 0;
-    if (!leader || tq != 0) tr = nullptr;
+    const bool leader = true;
+    if (lane != 0) {
+        __syncwarp();
+        return;
+    }
+    if (tq != 0) tr = nullptr;
     auto full_bar = [&](int p) { return smem_u32(&aux->bar_full[ring_slot<T>(p)]); };
     auto empty_bar = [&](int p) { return smem_u32(&aux->bar_empty[ring_slot<T>(p)]); };
     auto wait_tile = [&](int p0, unsigned site) {
         for (int pc = 0; pc < T::PIECES; ++pc)
-            if (!mbar_wait(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
+            if (!mbar_wait_lane(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
                 return false;
         return true;
     };
@@ -335,7 +341,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     uint64_t kd[T::PIECES];
 
     if (w.n_max > 0) do {
-        if (!mbar_wait(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         if constexpr (T::NQ == 2) {
             // one issuing warp alternates the tiles: PV_0(j), S_0(j+1),
             // PV_1(j), S_1(j+1); each softmax overlaps the other tile's MMAs
@@ -351,7 +357,6 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 }
             }
             release_tile(0, false);
-            __syncwarp();
             bool ok = true;
             for (int j = 0; j < w.n_max && ok; ++j) {
                 const int posV = (2 * j + 1) * T::PIECES;
@@ -363,7 +368,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j >= w.n_kv[t]) continue;
-                    if (!mbar_wait(smem_u32(&aux->bar_p_ready[t]), ph, wc,
+                    if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[t]), ph, wc,
                                    kErrWaitTimeout | kSiteMmaP)) {
                         ok = false;
                         break;
@@ -377,7 +382,6 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                     }
                     if (t == 1) release_tile(posV, false);   // V_j fully consumed
                     trace_mark(tr, kTrMma, j, 2 + 3 * t);
-                    __syncwarp();
                     if (j + 1 < w.n_kv[t]) {
                         if (!k_next_ready) {
                             if (!wait_tile(posK, kSiteMmaK)) { ok = false; break; }
@@ -386,7 +390,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                             kdesc(posK, kd);
                         }
                         // S_t(j+1) overwrites P_t(j): PV_t(j) must have completed
-                        if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), ph, wc,
+                        if (!mbar_wait_lane(smem_u32(&aux->bar_pv_done[t]), ph, wc,
                                        kErrWaitTimeout | kSiteMmaPv)) {
                             ok = false;
                             break;
@@ -398,12 +402,10 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                             tc_commit(smem_u32(&aux->bar_s_full[t]));
                         }
                         trace_mark(tr, kTrMma, j, 9 + t);
-                        __syncwarp();
                     }
                 }
                 if (ok && j + 1 < w.n_max) release_tile(posK, false);
                 trace_mark(tr, kTrMma, j, 8);
-                __syncwarp();
             }
         } else {
             if (!wait_tile(0, kSiteMmaK)) break;
@@ -414,7 +416,6 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 tc_commit(smem_u32(&aux->bar_s_full[0]));
             }
             release_tile(0, false);
-            __syncwarp();
             for (int j = 0; j < w.n_max; ++j) {
                 const int posV = (2 * j + 1) * T::PIECES;
                 const int posK = (2 * j + 2) * T::PIECES;
@@ -422,7 +423,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 // P(j-1), so PV(j-1) must have completed
                 if (j + 1 < w.n_max) {
                     if (!wait_tile(posK, kSiteMmaK)) break;
-                    if (j >= 1 && !mbar_wait(smem_u32(&aux->bar_pv_done[0]),
+                    if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[0]),
                                              (uint32_t)((j - 1) & 1), wc,
                                              kErrWaitTimeout | kSiteMmaPv))
                         break;
@@ -433,11 +434,10 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                         tc_commit(smem_u32(&aux->bar_s_full[(j + 1) & 1]));
                     }
                     release_tile(posK, false);
-                    __syncwarp();
                 }
                 if (!wait_tile(posV, kSiteMmaV)) break;
                 trace_mark(tr, kTrMma, j, 0);
-                if (!mbar_wait(smem_u32(&aux->bar_p_ready[0]), (uint32_t)(j & 1), wc,
+                if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[0]), (uint32_t)(j & 1), wc,
                                kErrWaitTimeout | kSiteMmaP))
                     break;
                 trace_mark(tr, kTrMma, j, 1);
@@ -452,13 +452,12 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 }
                 release_tile(posV, false);
                 trace_mark(tr, kTrMma, j, 2);
-                __syncwarp();
             }
         }
     } while (0);
     // All MMAs issued by this warp must have completed before tensor memory
     // is freed.
-    if (leader) {
+    {
         const uint32_t drain = smem_u32(&aux->bar_drain[tq]);
         tc_commit(drain);
         mbar_wait_drain(drain, 0, a.wait_limit_ns);
@@ -485,7 +484,6 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
     float l_run = 0.f;         // running row_sum in that basis
     const uint32_t mb_full = smem_u32(&aux->bar_mb_full[t]);
-    const uint32_t mb_empty = smem_u32(&aux->bar_mb_empty[t]);
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
         const int sb = (T::NSBUF == 2) ? (j & 1) : 0;
@@ -534,11 +532,10 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
             alpha = ex2_approx(m_run - m_new);   // 0 when m_run = -inf
             m_run = m_new;
         }
-        // mailbox message j: the rebase factor, for the correction warpgroup
-        if (!mbar_wait(mb_empty, (uint32_t)((j & 1) ^ 1), wc, kErrWaitTimeout | kSiteSmMbox)) {
-            ok = false;
-            break;
-        }
+        // Mailbox message j: the rebase factor, for the correction warpgroup.
+        // The slot is free without a handshake: S_t(j) was issued after
+        // PV_t(j-1), which waited for the correction's arrive on P-ready
+        // (j-1), made after it had read message j-1.
         aux->mb_alpha[t][r] = alpha;
         mbar_arrive_warp(mb_full);
         trace_mark(tr, trole, j, 3);
@@ -566,25 +563,26 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
                                      : make_float2(ex2_approx(x.x), ex2_approx(x.y));
                 rs[c & 3] = fadd2(rs[c & 3], p);
                 pk[c >> 5][c & 31] = pack_bf16x2(p.x, p.y);
+                // keys 0..63 go to columns 64..95, whose scores are already in
+                // registers: store them early to shorten the live range
+                if (c == 31) tmem_st32(lane_base + scol + 64, pk[0]);
             }
         }
         const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
         const float2 rsum = fadd2(rs01, rs23);
         l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
         trace_mark(tr, trole, j, 4);
-        tmem_st32(lane_base + scol + 64, pk[0]);
+        if (warp_masked) tmem_st32(lane_base + scol + 64, pk[0]);
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));
         trace_mark(tr, trole, j, 5);
     }
-    if (ok) {   // final message nk: row statistics for the epilogue
-        if (mbar_wait(mb_empty, (uint32_t)((nk & 1) ^ 1), wc, kErrWaitTimeout | kSiteSmMbox)) {
-            aux->mb_l[t][r] = l_run;
-            aux->mb_m[t][r] = m_run;
-            mbar_arrive_warp(mb_full);
-        }
+    if (ok) {   // final message nk: row statistics for the epilogue (own slots)
+        aux->mb_l[t][r] = l_run;
+        aux->mb_m[t][r] = m_run;
+        mbar_arrive_warp(mb_full);
     }
 }
 
@@ -610,7 +608,6 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             }
             trace_mark(tr, kTrCorr, j, 4 * t);
             const float alpha = aux->mb_alpha[t][r];
-            mbar_arrive_warp(smem_u32(&aux->bar_mb_empty[t]));
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
                 if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((j - 1) & 1), wc,
@@ -732,7 +729,6 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             mbar_init(smem_u32(&aux->bar_p_ready[t]), 8);   // 4 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_pv_done[t]), 1);
             mbar_init(smem_u32(&aux->bar_mb_full[t]), 4);
-            mbar_init(smem_u32(&aux->bar_mb_empty[t]), 4);
             mbar_init(smem_u32(&aux->bar_epi[t]), 4);
         }
         mbar_init(smem_u32(&aux->bar_drain[0]), 1);

@@ -35,6 +35,38 @@ METRIC = "prefill fwd TFLOPS & % bf16 tensor peak; decode HBM GB/s & % peak (1×
 FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# the ncu captures summarised under profiles/, keyed by the sha256 of the
+# kernel sources at capture time.  A source change makes the entry stale, and
+# stale entries are reported as null.
+KERNEL_SOURCES = {
+    "prefill": ["attention_forward_blackwell_gb300/csrc/prefill.cuh",
+                "attention_forward_blackwell_gb300/csrc/ptx.cuh",
+                "attention_forward_blackwell_gb300/csrc/common.cuh"],
+    "decode": ["attention_forward_blackwell_gb300/csrc/decode.cu",
+               "attention_forward_blackwell_gb300/csrc/ptx.cuh",
+               "attention_forward_blackwell_gb300/csrc/common.cuh"],
+}
+CAPTURED_TRAFFIC = {
+    # kernel: (sources sha256, bytes per launch, profile summary)
+}
+
+
+def sources_hash(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(kernel):
+    entry = CAPTURED_TRAFFIC.get(kernel)
+    if entry is None or entry[0] != sources_hash(kernel):
+        return None
+    return entry[1]
+
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
@@ -260,7 +292,8 @@ def run_ours(args, dist):
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / peaks["bf16_tflops"], 4),
                      "peak_source": peaks["source"] + " (burst bf16 GEMM)",
-                     "traffic": None},
+                     "traffic": captured_traffic("prefill"),
+                     "kernel_sources_sha256": sources_hash("prefill")[:16]},
         "gpu_launches": 2 * K,
         "clocks": clk,
     }
@@ -350,7 +383,8 @@ def run_decode(args, torch, binding, inputs, W, peaks, dev, dist):
             "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"], "traffic": None},
+                         "peak_source": peaks["source"], "traffic": captured_traffic("decode"),
+                         "kernel_sources_sha256": sources_hash("decode")[:16]},
             "gpu_launches": 2 * K,
             "l2": "flushed between steps (512 MiB write outside the timed events)"}
 
