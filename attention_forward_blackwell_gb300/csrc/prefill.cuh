@@ -87,12 +87,19 @@ struct PrefillTraits {
     static constexpr uint32_t TMEM_COLS = 512;
     // Register split (threads x registers after setmaxnreg must not exceed
     // the launch allocation: 512 x 128 for NQ = 2, 384 x 168 for NQ = 1).
+    // Every target differs from the launch count (increase or decrease).
     static constexpr uint32_t REG_SOFTMAX = (NQ == 2) ? 168 : 240;
     static constexpr uint32_t REG_CORR = (NQ == 2) ? 88 : 88;
     static constexpr uint32_t REG_OTHER = (NQ == 2) ? 88 : 80;
+    static constexpr uint32_t LAUNCH_REGS = (NQ == 2) ? 128 : 168;
+    static_assert(REG_SOFTMAX > LAUNCH_REGS && REG_CORR < LAUNCH_REGS && REG_OTHER < LAUNCH_REGS,
+                  "setmaxnreg targets must move away from the launch allocation");
+    static_assert(4 * NQ * 32 * REG_SOFTMAX + 4 * 32 * REG_CORR + 4 * 32 * REG_OTHER <=
+                      THREADS * LAUNCH_REGS,
+                  "register split exceeds the launch allocation");
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
-    static constexpr int SMEM_AUX = 4096;
+    static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
     static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX;
 
     __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * 128); }
@@ -109,7 +116,11 @@ struct PrefillAux {
     uint64_t bar_s_full[2];        // NQ = 2: per tile; NQ = 1: per score buffer
     uint64_t bar_p_ready[T::NQ];   // P_t(j) written and O_t rebased (softmax + correction)
     uint64_t bar_pv_done[T::NQ];
-    uint64_t bar_mb_full[T::NQ];
+    uint64_t bar_mb_full[T::NQ];   // mailbox message j (alpha) posted
+    uint64_t bar_fin[T::NQ];       // final row statistics posted (own barrier: the
+                                   // final message does not wait for message nk-1
+                                   // to be consumed, so sharing mb_full could let
+                                   // it complete two phases ahead of its reader)
     uint64_t bar_epi[T::NQ];       // staging of O_t in shared memory complete
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
@@ -579,10 +590,10 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));
         trace_mark(tr, trole, j, 5);
     }
-    if (ok) {   // final message nk: row statistics for the epilogue (own slots)
+    if (ok) {   // final row statistics for the epilogue (own slots, own barrier)
         aux->mb_l[t][r] = l_run;
         aux->mb_m[t][r] = m_run;
-        mbar_arrive_warp(mb_full);
+        mbar_arrive_warp(smem_u32(&aux->bar_fin[t]));
     }
 }
 
@@ -635,8 +646,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
     // epilogue: O / row_sum -> bf16 -> shared (Q tile's space, 128-byte swizzled) -> TMA store
     for (int t = 0; t < T::NQ && ok; ++t) {
         const int nk = w.n_kv[t];
-        if (!mbar_wait(smem_u32(&aux->bar_mb_full[t]), (uint32_t)(nk & 1), wc,
-                       kErrWaitTimeout | kSiteEpiMbox)) {
+        if (!mbar_wait(smem_u32(&aux->bar_fin[t]), 0, wc, kErrWaitTimeout | kSiteEpiMbox)) {
             ok = false;
             break;
         }
@@ -707,6 +717,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                    const PrefillArgs args) {
     using T = PrefillTraits<D>;
+    static_assert(sizeof(PrefillAux<T>) <= T::SMEM_AUX, "auxiliary shared block too large");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sQ = (raw + 1023u) & ~1023u;   // 1024-aligned: swizzle atoms
@@ -729,6 +740,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             mbar_init(smem_u32(&aux->bar_p_ready[t]), 8);   // 4 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_pv_done[t]), 1);
             mbar_init(smem_u32(&aux->bar_mb_full[t]), 4);
+            mbar_init(smem_u32(&aux->bar_fin[t]), 4);
             mbar_init(smem_u32(&aux->bar_epi[t]), 4);
         }
         mbar_init(smem_u32(&aux->bar_drain[0]), 1);

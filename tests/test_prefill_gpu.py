@@ -167,3 +167,24 @@ def test_wait_timeout_selftest_reports_and_recovers():
     assert binding.get_device_error() == binding.FA_OK     # cleared
     x = inputs.make_inputs(1, 1, 1, 128, 128, 64, tag=1, device="cuda")
     _full_check(x, 0.125, False, "after timeout")
+
+
+@pytest.mark.parametrize("B,Hq,Sq,Sk,d,causal", [
+    (1, 1, 128, 128, 64, False),    # one key tile per query tile
+    (1, 1, 257, 1, 64, False),      # one key, a CTA whose second tile has no rows
+    (1, 2, 300, 300, 128, True),    # the two query tiles finish after different counts
+    (1, 4, 600, 200, 256, True),    # d = 256, rows that see no key
+])
+def test_barrier_protocol_stress(B, Hq, Sq, Sk, d, causal):
+    """Many back-to-back launches of shapes whose pipelines are short (one or
+    two key tiles), where a message that runs ahead of its reader would show
+    up as a wait time-out: no launch may record one, and every result stays
+    equal to the first."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(B, Hq, Hq, Sq, Sk, d, tag=450 + Sq, device="cuda")
+    o0, l0 = _run(x, 1.0 / math.sqrt(d), causal)
+    for _ in range(40):
+        o, l = binding.prefill(x.q, x.k, x.v, scale=1.0 / math.sqrt(d), causal=causal)
+    torch.cuda.synchronize()
+    check_device_error()
+    assert torch.equal(o, o0) and torch.equal(l, l0)
