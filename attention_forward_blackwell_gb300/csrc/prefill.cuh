@@ -75,10 +75,9 @@ struct PrefillTraits {
     static constexpr int NSLOT = (D == 64) ? 8 : 4;
     static constexpr int KSTEPS = D / 16;              // score MMA steps of K = 16
     static constexpr int D_COLS = D;                   // O accumulator columns
-    // Value MMA N per instruction.  head_dim 96 runs N = 128: its second
-    // 64-column V chunk is half zero-filled by TMA (columns past d read as
-    // zero), so O columns 96..127 stay zero and are never stored.
-    static constexpr int PV_N = (D == 96) ? 128 : ((D <= 128) ? D : 128);
+    // Value MMA N per instruction (head_dim 96: N = 96, i.e. one full and one
+    // half 64-column chunk of the MN-major V tile).
+    static constexpr int PV_N = (D <= 128) ? D : 128;
     static constexpr int NUM_WARPS = (NQ + 2) * 4;
     static constexpr int THREADS = NUM_WARPS * 32;
     static constexpr int CORR_WG = NQ;

@@ -49,6 +49,12 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
+    "prefill": ("ef073acfda8b5f3f741aa66a69108e415256c80d577b2e3f4587a97e0180b8f3",
+                114902016, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    # captured at batch 16 (463.64 MB) and scaled to batch 64 by the
+    # algorithmic bytes of the two batches
+    "decode": ("ccee9490d466358969a2ce27889455468df8582642f5d88bbe9ebe7b648ca774",
+               2205000000, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 
@@ -76,6 +82,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--decode-batch", type=int, default=None,
+                   help="batch of the decode leg (default: the workload's 64); a "
+                        "smaller batch keeps profiler captures small")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU (oracle) baseline sample")
     return p.parse_args(argv)
@@ -349,6 +358,9 @@ def run_e2e(args, torch, binding, x, w, f_n, f_c, dist):
 
 def run_decode(args, torch, binding, inputs, W, peaks, dev, dist):
     w = W.DECODE
+    if args.decode_batch is not None and args.decode_batch != w.B:
+        import dataclasses
+        w = dataclasses.replace(w, B=int(args.decode_batch), name=f"{w.name}_batch{args.decode_batch}")
     x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device=dev,
                            lengths=w.lengths)
     lens = x.seqlens_k.cpu().tolist()
@@ -383,7 +395,8 @@ def run_decode(args, torch, binding, inputs, W, peaks, dev, dist):
             "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1),
                          "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": round(per_gpu / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"], "traffic": captured_traffic("decode"),
+                         "peak_source": peaks["source"],
+                         "traffic": captured_traffic("decode") if w.B == W.DECODE.B else None,
                          "kernel_sources_sha256": sources_hash("decode")[:16]},
             "gpu_launches": 2 * K,
             "l2": "flushed between steps (512 MiB write outside the timed events)"}
