@@ -113,9 +113,11 @@ struct PrefillAux {
     uint64_t bar_full[T::NSLOT];
     uint64_t bar_empty[T::NSLOT];
     uint64_t bar_s_full[2];        // NQ = 2: per tile; NQ = 1: per score buffer
-    uint64_t bar_p_ready[T::NQ];   // P_t(j) written and O_t rebased (softmax + correction)
+    // P ready + O rebased and the rebase mailbox come in two copies, used by
+    // tile (NQ = 2) or by key-block parity (NQ = 1); see sig_idx.
+    uint64_t bar_p_ready[2];       // P(j) written and O rebased (softmax + correction)
     uint64_t bar_pv_done[T::NQ];
-    uint64_t bar_mb_full[T::NQ];   // mailbox message j (alpha) posted
+    uint64_t bar_mb_full[2];       // mailbox message j (alpha) posted
     uint64_t bar_fin[T::NQ];       // final row statistics posted (own barrier: the
                                    // final message does not wait for message nk-1
                                    // to be consumed, so sharing mb_full could let
@@ -125,7 +127,7 @@ struct PrefillAux {
     uint64_t bar_tail;             // producer-private: partial last value tile landed
     uint32_t tmem_base;
     int abort_flag;
-    float mb_alpha[T::NQ][128];
+    float mb_alpha[2][128];
     float mb_l[T::NQ][128];
     float mb_m[T::NQ][128];
 };
@@ -171,6 +173,22 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     }
     w.n_max = w.n_kv[T::NQ - 1];
     return w;
+}
+
+// Copy of the P-ready barrier and rebase mailbox that tile t's key block j
+// uses, and the phase parity of that block on it.  With two Q tiles (NQ = 2)
+// each tile has its own copy and every block is a phase: S_t(j+1) is issued
+// only after PV_t(j), so a tile's softmax never runs a block ahead of its
+// correction.  With one tile and two score buffers (NQ = 1) S(j+1) is issued
+// before PV(j), so the softmax can finish block j+1 before the correction has
+// handled block j; consecutive blocks then alternate between the two copies,
+// so that their arrivals and messages never share one (S(j+2) waits for
+// PV(j), hence for the correction's handling of block j).
+template <class T>
+__device__ __forceinline__ int sig_idx(int t, int j) { return T::NQ == 2 ? t : (j & 1); }
+template <class T>
+__device__ __forceinline__ uint32_t sig_par(int j) {
+    return T::NQ == 2 ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
 }
 
 // Ring position p (K_j piece c at p = 2 j PIECES + c, V_j at (2 j + 1) PIECES + c).
@@ -378,7 +396,8 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j >= w.n_kv[t]) continue;
-                    if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[t]), ph, wc,
+                    if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]),
+                                        sig_par<T>(j), wc,
                                    kErrWaitTimeout | kSiteMmaP)) {
                         ok = false;
                         break;
@@ -447,7 +466,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 }
                 if (!wait_tile(posV, kSiteMmaV)) break;
                 trace_mark(tr, kTrMma, j, 0);
-                if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[0]), (uint32_t)(j & 1), wc,
+                if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                kErrWaitTimeout | kSiteMmaP))
                     break;
                 trace_mark(tr, kTrMma, j, 1);
@@ -493,7 +512,6 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
     const int nk = w.n_kv[t];
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
     float l_run = 0.f;         // running row_sum in that basis
-    const uint32_t mb_full = smem_u32(&aux->bar_mb_full[t]);
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
         const int sb = (T::NSBUF == 2) ? (j & 1) : 0;
@@ -543,11 +561,12 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
             m_run = m_new;
         }
         // Mailbox message j: the rebase factor, for the correction warpgroup.
-        // The slot is free without a handshake: S_t(j) was issued after
-        // PV_t(j-1), which waited for the correction's arrive on P-ready
-        // (j-1), made after it had read message j-1.
-        aux->mb_alpha[t][r] = alpha;
-        mbar_arrive_warp(mb_full);
+        // The slot is free without a handshake: S(j) was issued after the
+        // value MMA of the last block that used the same slot (j-1 for
+        // NQ = 2, j-2 for NQ = 1), which waited for the correction's arrive
+        // on P-ready, made after it had read that block's message.
+        aux->mb_alpha[sig_idx<T>(t, j)][r] = alpha;
+        mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, j)]));
         trace_mark(tr, trole, j, 3);
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sl2x2 = make_float2(sl2, sl2);
@@ -586,7 +605,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));
+        mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]));
         trace_mark(tr, trole, j, 5);
     }
     if (ok) {   // final row statistics for the epilogue (own slots, own barrier)
@@ -611,13 +630,13 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
     for (int j = 0; j < w.n_max && ok; ++j) {
         for (int t = 0; t < T::NQ; ++t) {
             if (j >= w.n_kv[t]) continue;
-            if (!mbar_wait(smem_u32(&aux->bar_mb_full[t]), (uint32_t)(j & 1), wc,
+            if (!mbar_wait(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, j)]), sig_par<T>(j), wc,
                            kErrWaitTimeout | kSiteCorrMbox)) {
                 ok = false;
                 break;
             }
             trace_mark(tr, kTrCorr, j, 4 * t);
-            const float alpha = aux->mb_alpha[t][r];
+            const float alpha = aux->mb_alpha[sig_idx<T>(t, j)][r];
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
                 if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((j - 1) & 1), wc,
@@ -638,7 +657,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive_warp(smem_u32(&aux->bar_p_ready[t]));   // O_t safe for PV_t(j)
+            mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]));   // O_t safe for PV_t(j)
             trace_mark(tr, kTrCorr, j, 4 * t + 1);
         }
     }
@@ -653,6 +672,16 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         const float l = aux->mb_l[t][r];
         const float m = aux->mb_m[t][r];
         if (nk > 0) {
+            // O is final once PV(nk-1) completed.  A parity wait is exact only
+            // while the barrier is at most one phase behind: with NQ = 2 the
+            // last score MMA waited for PV(nk-2), so one wait suffices; with
+            // NQ = 1 it only waited for PV(nk-3), so PV(nk-2) comes first.
+            if (T::NQ == 1 && nk >= 2 &&
+                !mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((nk - 2) & 1), wc,
+                           kErrWaitTimeout | kSiteEpiPv)) {
+                ok = false;
+                break;
+            }
             if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((nk - 1) & 1), wc,
                            kErrWaitTimeout | kSiteEpiPv)) {
                 ok = false;
@@ -735,10 +764,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&aux->bar_s_full[i]), 1);
         // warpgroup-to-warp signals: one elected arrive per warp
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&aux->bar_p_ready[i]), 8);   // 4 softmax + 4 correction warps
+            mbar_init(smem_u32(&aux->bar_mb_full[i]), 4);
+        }
         for (int t = 0; t < T::NQ; ++t) {
-            mbar_init(smem_u32(&aux->bar_p_ready[t]), 8);   // 4 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_pv_done[t]), 1);
-            mbar_init(smem_u32(&aux->bar_mb_full[t]), 4);
             mbar_init(smem_u32(&aux->bar_fin[t]), 4);
             mbar_init(smem_u32(&aux->bar_epi[t]), 4);
         }

@@ -82,9 +82,12 @@ struct WaitCtx {
 };
 
 // Records an error code once per device word and raises the CTA abort flag.
+// The word holds the code in bits 0-15 and the (linear) CTA index in bits
+// 16-31, so a time-out names the CTA whose wait gave up first.
 __device__ __forceinline__ void record_error(const WaitCtx& w, unsigned int code) {
     *w.abort_flag = 1;
-    atomicCAS(w.err_word, 0u, code);
+    const unsigned int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    atomicCAS(w.err_word, 0u, (code & 0xFFFFu) | ((cta & 0xFFFFu) << 16));
 }
 
 // One lane's bounded wait for the phase of `bar` with the given parity.

@@ -40,7 +40,9 @@
  *             on any error nothing is launched.  No C++ exception crosses
  *             this interface.  A kernel wait that exceeds its time limit
  *             makes the kernel finish early and records FA_ERR_TIMEOUT in a
- *             device error word, read by fa_get_device_error().
+ *             device error word, read by fa_get_device_error() (the word,
+ *             from fa_get_device_error_word(), holds the wait site in bits
+ *             0-15 and the CTA index in bits 16-31).
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
