@@ -37,6 +37,7 @@ SIGNATURES = {
     "fa_selftest_mma_tile": (_I, [_VP, _VP, _VP, _I, _I, _VP]),
     "fa_debug_prefill_trace": (_I, [_VP, _I]),
     "fa_selftest_exp2_poly": (_I, [_VP, _VP, _I, _VP]),
+    "fa_debug_prefill_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _VP]),
     "fa_version": (_I, []),
 }
 
@@ -197,6 +198,16 @@ def debug_prefill_trace(buf=None, block=0):
     st = lib().fa_debug_prefill_trace(_ptr(buf), int(block))
     if st != FA_OK:
         raise FaError(st, "fa_debug_prefill_trace")
+
+
+def debug_prefill_plan(batch, hq, sq, sk, head_dim, causal, num_sms):
+    """The prefill work split (host only, see fa.h): (n_full, n_tail, split)."""
+    out = (ctypes.c_int * 3)()
+    st = lib().fa_debug_prefill_plan(int(batch), int(hq), int(sq), int(sk), int(head_dim),
+                                     int(bool(causal)), int(num_sms), ctypes.addressof(out))
+    if st != FA_OK:
+        raise FaError(st, "fa_debug_prefill_plan")
+    return tuple(out)
 
 
 def selftest_exp2_poly(x, stream=None):

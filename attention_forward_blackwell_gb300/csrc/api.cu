@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -76,6 +77,14 @@ const DeviceInfo* device_info() {
         di.ready = true;
     }
     return &di;
+}
+
+// Tags of the split-unit arrival counters: a 48-bit value no earlier launch
+// of this process used, so counters left in reused scratch never match.
+unsigned long long next_prefill_epoch() {
+    static std::atomic<unsigned long long> counter{0};
+    const unsigned long long e = (counter.fetch_add(1) + 1) & ((1ull << 48) - 1);
+    return e == 0 ? 1 : e;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -211,6 +220,7 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
         !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
         return FA_ERR_INVALID_ARG;
     PrefillArgs& a = p.args;
+    a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.seqlens_k = seqlens_k;
     a.err_word = di->err_word;
@@ -228,6 +238,28 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     a.trace_block = g_trace_block;
     p.head_dim = head_dim;
     p.causal = causal ? 1 : 0;
+    // work split: whole units, then the last partial wave's units in pieces
+    const long long units = (long long)batch * hq * a.num_mblk;
+    if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    a.nk = (sk + 127) / 128;
+    const PrefillPlan plan = plan_prefill(units, a.nk, p.causal, di->num_sms);
+    a.n_full = plan.n_full;
+    a.split = plan.split;
+    p.n_tail = plan.n_tail;
+    void* ws = nullptr;
+    if (plan.n_tail > 0) {
+        const int nq = rows_per_cta / 128;
+        const size_t pieces = (size_t)plan.n_tail * plan.split;
+        const size_t part_o = pieces * nq * head_dim * 128 * sizeof(float);
+        const size_t part_ml = pieces * nq * 2 * 128 * sizeof(float);
+        const size_t counts = (size_t)plan.n_tail * sizeof(unsigned long long);
+        if (cudaMallocAsync(&ws, part_o + part_ml + counts, s) != cudaSuccess) return FA_ERR_CUDA;
+        a.part_o = static_cast<float*>(ws);
+        a.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + part_o);
+        a.part_count =
+            reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) + part_o + part_ml);
+        a.epoch = next_prefill_epoch();
+    }
     cudaError_t e;
     switch (head_dim) {
         case 64: e = launch_prefill_d64(p, s); break;
@@ -235,6 +267,7 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
         case 128: e = launch_prefill_d128(p, s); break;
         default: e = launch_prefill_d256(p, s); break;
     }
+    if (ws != nullptr && cudaFreeAsync(ws, s) != cudaSuccess) return FA_ERR_CUDA;
     return from_cuda(e);
 }
 
@@ -337,6 +370,23 @@ fa_status fa_debug_prefill_trace(unsigned long long* buf, int block) {
     return FA_OK;
 }
 
-int fa_version(void) { return 100; }
+fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                int num_sms, int* out) {
+    if (!out || batch <= 0 || hq <= 0 || sq <= 0 || sk <= 0 || batch > 65535 || hq > 65535 ||
+        num_sms < 1)
+        return FA_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
+        return FA_ERR_INVALID_ARG;
+    const int rows = prefill_rows_per_cta(head_dim);
+    const long long units = (long long)batch * hq * ((sq + rows - 1) / rows);
+    if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    const PrefillPlan p = plan_prefill(units, (sk + 127) / 128, causal ? 1 : 0, num_sms);
+    out[0] = p.n_full;
+    out[1] = p.n_tail;
+    out[2] = p.split;
+    return FA_OK;
+}
+
+int fa_version(void) { return 110; }
 
 }  // extern "C"

@@ -19,12 +19,27 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 // ----------------------------------------------------------- prefill ----
 
 struct PrefillArgs {
+    uint16_t* o;                // [B, Hq, Sq, d] bf16 bits (written directly by merges)
     float* lse;                 // [B, Hq, Sq] fp32
     const int* seqlens_k;       // [B] int32 or nullptr
     unsigned int* err_word;     // device error word
     int B, Hq, Hkv, Sq, Sk;
     int group;                  // Hq / Hkv
-    int num_mblk;               // CTAs along the query axis per (b, h)
+    int num_mblk;               // query blocks (units) per (b, h)
+    // Work split (see prefill_work): CTAs [0, n_full) process whole units;
+    // each later unit is split into `split` pieces of its nk key blocks.
+    int n_full;
+    int split;
+    int nk;                     // key blocks of a unit, ceil(Sk / 128)
+    // Scratch of the split units (nullptr when nothing is split): partial O
+    // of every piece, [pieces][NQ][d / 4][128][4] fp32, its row max and row
+    // sum, [pieces][NQ][2][128] fp32, and one arrival counter per split unit,
+    // tagged with `epoch` (a value no earlier launch used) so that stale
+    // counter contents never count.
+    float* part_o;
+    float* part_ml;
+    unsigned long long* part_count;
+    unsigned long long epoch;
     float scale_log2;           // scale * log2(e)
     unsigned long long wait_limit_ns;
     // Debug trace (nullptr in normal use): one thread per role of CTA
@@ -42,12 +57,43 @@ enum TraceRole { kTrMma = 0, kTrSoftmax0 = 1, kTrSoftmax1 = 2, kTrCorr = 3, kTrL
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;   // 3-D maps {d, S, B*H}, box {64, 128, 1}
     PrefillArgs args;
+    int n_tail;                 // split units
     int head_dim;
     int causal;
 };
 
-// Query rows handled by one CTA of the prefill kernel for a head dimension.
+// Query rows of one prefill unit (query block) for a head dimension.
 inline int prefill_rows_per_cta(int head_dim) { return head_dim <= 128 ? 256 : 128; }
+
+// Split of the prefill work over the grid.  With units of equal work
+// (non-causal), the units beyond the last full wave of `ctas` whole-unit
+// CTAs (all units if there are fewer than `ctas`) are cut into `split`
+// pieces along the key axis: the largest split whose pieces all run in one
+// wave (tail * split <= ctas) with at least 8 key blocks per piece and at
+// most 8 pieces, so that the last wave is `split` times shorter (measured on
+// GB300: more pieces than one wave holds, or shorter pieces, lose more to
+// per-CTA set-up and to the merge than they gain).  Causal units start
+// heaviest first and are not split.
+struct PrefillPlan {
+    int n_full;   // CTAs that process a whole unit
+    int n_tail;   // units processed in pieces
+    int split;    // pieces per such unit (1: nothing is split)
+};
+
+inline PrefillPlan plan_prefill(long long units, int nk, int causal, int ctas) {
+    PrefillPlan p{(int)units, 0, 1};
+    if (causal || units <= 0 || ctas <= 0) return p;
+    const long long tail = units % ctas;
+    if (tail == 0) return p;
+    long long k = ctas / tail;
+    if (k > nk / 8) k = nk / 8;
+    if (k > 8) k = 8;
+    if (k < 2) return p;
+    p.n_full = (int)(units - tail);
+    p.n_tail = (int)tail;
+    p.split = (int)k;
+    return p;
+}
 
 cudaError_t launch_prefill_d64(const PrefillLaunch& p, cudaStream_t s);
 cudaError_t launch_prefill_d96(const PrefillLaunch& p, cudaStream_t s);

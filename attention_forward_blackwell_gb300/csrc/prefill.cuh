@@ -116,7 +116,7 @@ struct PrefillAux {
     // P ready + O rebased and the rebase mailbox come in two copies, used by
     // tile (NQ = 2) or by key-block parity (NQ = 1); see sig_idx.
     uint64_t bar_p_ready[2];       // P(j) written and O rebased (softmax + correction)
-    uint64_t bar_pv_done[T::NQ];
+    uint64_t bar_pv_done[2];       // value MMA completed (copies as for P-ready)
     uint64_t bar_mb_full[2];       // mailbox message j (alpha) posted
     uint64_t bar_fin[T::NQ];       // final row statistics posted (own barrier: the
                                    // final message does not wait for message nk-1
@@ -125,8 +125,11 @@ struct PrefillAux {
     uint64_t bar_epi[T::NQ];       // staging of O_t in shared memory complete
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
+    uint64_t bar_split_a;          // piece of a split unit: partial result written (4 warps)
+    uint64_t bar_split_b;          // arrival counted; merge decision posted
     uint32_t tmem_base;
     int abort_flag;
+    int merge_last;
     float mb_alpha[2][128];
     float mb_l[T::NQ][128];
     float mb_m[T::NQ][128];
@@ -136,8 +139,12 @@ struct PrefillAux {
 enum : unsigned int {
     kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
-    kSiteEpiStage
+    kSiteEpiStage, kSiteSplitA, kSiteSplitB
 };
+
+// Recorded if a piece's arrival could not be counted (never expected: every
+// failed compare-and-swap means another piece of the unit was counted).
+constexpr unsigned int kErrSplitCount = 0x2001u;
 
 // Debug trace stamp (SM clock) by the calling thread, if tracing this CTA.
 __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int j, int e) {
@@ -146,18 +153,50 @@ __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int
 }
 
 // Per-CTA work coordinates, computed identically by every thread.
+//
+// The grid is one-dimensional.  Its first n_full CTAs each process a whole
+// unit (batch entry, query head, query block), in the order query block
+// (fastest; heaviest first when causal), head, batch entry.  The remaining
+// units (the last, partial wave of a grid of whole units) are each split
+// along the key axis into `split` pieces of consecutive key blocks, one CTA
+// per piece, so that the last wave is `split` times shorter; the pieces write
+// partial results and the last one to finish merges them (tail_merge).
+// Key-block counters below are local to the CTA's piece: block j of the
+// piece is key block kb + j.
 struct PrefillWork {
     int b, h, hk, row0, L, off;
-    int n_kv[2];   // K/V tiles visited by Q tile 0 / 1
+    int n_kv[2];   // key blocks of this piece visited by Q tile 0 / 1
     int n_max;
+    int kb;        // first key block of the piece (0 for a whole unit)
+    int piece;     // -1 for a whole unit, else the piece's scratch slot
+    int tail;      // tail unit of the piece (its merge counter)
 };
 
 template <class T, bool CAUSAL>
 __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     PrefillWork w;
-    const int mblk = CAUSAL ? (a.num_mblk - 1 - (int)blockIdx.x) : (int)blockIdx.x;
-    w.h = blockIdx.y;
-    w.b = blockIdx.z;
+    const int c = (int)blockIdx.x;
+    int u, ke;
+    if (c < a.n_full) {
+        u = c;
+        w.kb = 0;
+        ke = 0x7fffffff;
+        w.piece = -1;
+        w.tail = -1;
+    } else {
+        const int q = c - a.n_full;
+        const int k = q % a.split;
+        w.tail = q / a.split;
+        u = a.n_full + w.tail;
+        w.kb = (int)((long long)k * a.nk / a.split);
+        ke = (int)((long long)(k + 1) * a.nk / a.split);
+        w.piece = q;
+    }
+    const int x = u % a.num_mblk;
+    const int hb = u / a.num_mblk;
+    const int mblk = CAUSAL ? (a.num_mblk - 1 - x) : x;
+    w.h = hb % a.Hq;
+    w.b = hb / a.Hq;
     w.hk = w.h / a.group;
     int L = a.Sk;
     if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[w.b], a.Sk));
@@ -169,21 +208,28 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     for (int t = 0; t < T::NQ; ++t) {
         int last = L - 1;   // last key any row of the tile can see
         if (CAUSAL) last = min(last, w.row0 + (t + 1) * T::BM - 1 + w.off);
-        w.n_kv[t] = last >= 0 ? last / T::BN + 1 : 0;
+        const int n = last >= 0 ? last / T::BN + 1 : 0;
+        const int cnt = min(n, ke) - w.kb;
+        w.n_kv[t] = cnt > 0 ? cnt : 0;
     }
-    w.n_max = w.n_kv[T::NQ - 1];
+    w.n_max = max(w.n_kv[0], w.n_kv[T::NQ - 1]);
     return w;
 }
 
-// Copy of the P-ready barrier and rebase mailbox that tile t's key block j
-// uses, and the phase parity of that block on it.  With two Q tiles (NQ = 2)
+// Copy of the P-ready barrier, rebase mailbox and value-MMA completion
+// barrier that tile t's key block j uses, and the phase parity of that block
+// on it.  With two Q tiles (NQ = 2)
 // each tile has its own copy and every block is a phase: S_t(j+1) is issued
 // only after PV_t(j), so a tile's softmax never runs a block ahead of its
 // correction.  With one tile and two score buffers (NQ = 1) S(j+1) is issued
 // before PV(j), so the softmax can finish block j+1 before the correction has
 // handled block j; consecutive blocks then alternate between the two copies,
 // so that their arrivals and messages never share one (S(j+2) waits for
-// PV(j), hence for the correction's handling of block j).
+// PV(j), hence for the correction's handling of block j).  The same holds for
+// the completion of value MMAs: a parity wait is exact only while its barrier
+// is at most one phase behind, and with NQ = 1 two value MMAs can be in
+// flight; on alternating copies the previous PV of a copy (PV(j-2)) has
+// always been waited for by the time PV(j) is (S(j) waits for PV(j-2)).
 template <class T>
 __device__ __forceinline__ int sig_idx(int t, int j) { return T::NQ == 2 ? t : (j & 1); }
 template <class T>
@@ -250,7 +296,8 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
             break;
         trace_mark(tr, kTrLoad, p >> 3, p & 7);
         const uint32_t full = smem_u32(&aux->bar_full[slot]);
-        const int rv = w.L - j * T::BN;   // valid rows of this tile
+        const int jk = w.kb + j;          // key block
+        const int rv = w.L - jk * T::BN;  // valid rows of this tile
         if (kv == 1 && j == w.n_max - 1 && rv < T::BN) {
             // Partial last value tile: rows [rv, BN) may hold anything (and a
             // zero probability times a non-finite value would poison O), so
@@ -261,7 +308,7 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 #pragma unroll
                 for (int c = 0; c < T::SLOT_CH; ++c)
                     tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, tm_v,
-                                (pc * T::SLOT_CH + c) * 64, j * T::BN, w.b * a.Hkv + w.hk, tail);
+                                (pc * T::SLOT_CH + c) * 64, jk * T::BN, w.b * a.Hkv + w.hk, tail);
             }
             if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail)) break;
             zero_value_tail<T>(sRing + slot * T::SLOT, rv);
@@ -272,7 +319,7 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 #pragma unroll
             for (int c = 0; c < T::SLOT_CH; ++c)
                 tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, m, (pc * T::SLOT_CH + c) * 64,
-                            j * T::BN, w.b * a.Hkv + w.hk, full);
+                            jk * T::BN, w.b * a.Hkv + w.hk, full);
         }
         __syncwarp();
         issued = p + 1;
@@ -452,9 +499,9 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 // P(j-1), so PV(j-1) must have completed
                 if (j + 1 < w.n_max) {
                     if (!wait_tile(posK, kSiteMmaK)) break;
-                    if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[0]),
-                                             (uint32_t)((j - 1) & 1), wc,
-                                             kErrWaitTimeout | kSiteMmaPv))
+                    if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                                                  sig_par<T>(j - 1), wc,
+                                                  kErrWaitTimeout | kSiteMmaPv))
                         break;
                     tc_fence_after();
                     kdesc(posK, kd);
@@ -477,7 +524,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                         issue_value<T>(tmem + T::o_col(0) + nh * 128,
                                        tmem + T::s_col(j & 1) + 64, vd0 + slot_off(posV + nh),
                                        idesc_v, j == 0);
-                    tc_commit(smem_u32(&aux->bar_pv_done[0]));
+                    tc_commit(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j)]));
                 }
                 release_tile(posV, false);
                 trace_mark(tr, kTrMma, j, 2);
@@ -508,6 +555,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
     const int row = w.row0 + t * T::BM + r;
     int lim = w.L - 1;                                       // last visible key of this row
     if (CAUSAL) lim = min(lim, row + w.off);
+    lim -= w.kb * T::BN;   // keys counted from the piece's first key block
     const float sl2 = a.scale_log2;
     const int nk = w.n_kv[t];
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
@@ -536,7 +584,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
         // mask: only tiles that reach past this row's last visible key
-        const int kv0 = j * T::BN;
+        const int kv0 = j * T::BN;   // relative to the piece's first key (lim is too)
         const bool masked = lim - kv0 < T::BN - 1;
         const bool warp_masked = __any_sync(0xffffffffu, masked);
         if (masked) {
@@ -574,8 +622,10 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
         uint32_t pk[2][32];
-        if (warp_masked) {
-            // masked entries are -inf and must give exactly 0: hardware ex2 only
+        if (kUsePolyExp2 && warp_masked) {
+            // masked entries are -inf and must give exactly 0: hardware ex2
+            // only (without the polynomial option both loops are the same,
+            // and only the one below is compiled)
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
                 const float2 x = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, nbase);
@@ -601,7 +651,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         const float2 rsum = fadd2(rs01, rs23);
         l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
         trace_mark(tr, trole, j, 4);
-        if (warp_masked) tmem_st32(lane_base + scol + 64, pk[0]);
+        if (kUsePolyExp2 && warp_masked) tmem_st32(lane_base + scol + 64, pk[0]);
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
@@ -616,6 +666,99 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
 }
 
 // ---------------------------------------------------- correction/epilogue ----
+
+// Stores 32 columns of one output row as bf16: O = v * inv_l.
+__device__ __forceinline__ void store_o32(uint16_t* orow, const float (&v)[32], float inv_l) {
+    uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 x;
+        x.x = pack_bf16x2(v[8 * q + 0] * inv_l, v[8 * q + 1] * inv_l);
+        x.y = pack_bf16x2(v[8 * q + 2] * inv_l, v[8 * q + 3] * inv_l);
+        x.z = pack_bf16x2(v[8 * q + 4] * inv_l, v[8 * q + 5] * inv_l);
+        x.w = pack_bf16x2(v[8 * q + 6] * inv_l, v[8 * q + 7] * inv_l);
+        dst[q] = x;
+    }
+}
+
+// Arrival of a piece of a split unit (after its partial result is in
+// scratch) and, for the last piece to arrive, the merge: the pieces' O, row
+// max and row sum are rebased to their common max and added (the same
+// recurrence as between key blocks), then O / row_sum and LSE are stored.
+// No CTA waits for another: the counter tells each piece whether it is last.
+template <class T>
+__device__ void tail_merge(const PrefillArgs& a, const PrefillWork& w, PrefillAux<T>* aux, int r,
+                           const WaitCtx& wc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    mbar_arrive_warp(smem_u32(&aux->bar_split_a));   // this warp's stores issued
+    bool ok = true;
+    if (warp == T::CORR_WG * 4) {
+        ok = mbar_wait(smem_u32(&aux->bar_split_a), 0, wc, kErrWaitTimeout | kSiteSplitA);
+        if (ok && lane == 0) {
+            __threadfence();   // this piece's stores (all four warps) before the count
+            unsigned long long* cp = a.part_count + w.tail;
+            const unsigned long long tag = a.epoch << 16;
+            unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cp);
+            unsigned long long arrived = 0;
+            for (int attempt = 0; attempt <= a.split; ++attempt) {
+                const unsigned long long cur = ((old >> 16) == a.epoch) ? (old & 0xffffull) : 0ull;
+                const unsigned long long prev = atomicCAS(cp, old, tag | (cur + 1));
+                if (prev == old) {
+                    arrived = cur + 1;
+                    break;
+                }
+                old = prev;
+            }
+            if (arrived == 0) record_error(wc, kErrSplitCount);
+            __threadfence();   // the other pieces' stores before this piece's loads
+            *reinterpret_cast<volatile int*>(&aux->merge_last) =
+                arrived == (unsigned long long)a.split ? 1 : 0;
+            mbar_arrive(smem_u32(&aux->bar_split_b));
+        }
+    }
+    if (!ok || !mbar_wait(smem_u32(&aux->bar_split_b), 0, wc, kErrWaitTimeout | kSiteSplitB)) return;
+    if (!*reinterpret_cast<volatile int*>(&aux->merge_last)) return;
+    const int s0 = w.tail * a.split;
+#pragma unroll 1
+    for (int t = 0; t < T::NQ; ++t) {
+        const int row = w.row0 + t * T::BM + r;
+        if (row >= a.Sq) continue;
+        auto ml_of = [&](int k) { return a.part_ml + ((size_t)(s0 + k) * T::NQ + t) * 2 * T::BM; };
+        float M = -INFINITY;
+        for (int k = 0; k < a.split; ++k) M = fmaxf(M, __ldcg(ml_of(k) + r));
+        float L = 0.f;
+        for (int k = 0; k < a.split; ++k) {
+            const float mk = __ldcg(ml_of(k) + r);
+            const float wk = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M);
+            L = fmaf(wk, __ldcg(ml_of(k) + T::BM + r), L);
+        }
+        const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
+        uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * T::D_COLS;
+#pragma unroll 1
+        for (int c32 = 0; c32 < T::D_COLS / 32; ++c32) {
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            for (int k = 0; k < a.split; ++k) {
+                const float mk = __ldcg(ml_of(k) + r);
+                const float wk = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M);
+                const float4* po = reinterpret_cast<const float4*>(
+                    a.part_o + ((size_t)(s0 + k) * T::NQ + t) * (T::D_COLS * T::BM));
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 x = __ldcg(po + (size_t)(c32 * 8 + q) * T::BM + r);
+                    acc[4 * q + 0] = fmaf(wk, x.x, acc[4 * q + 0]);
+                    acc[4 * q + 1] = fmaf(wk, x.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wk, x.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wk, x.w, acc[4 * q + 3]);
+                }
+            }
+            store_o32(orow + c32 * 32, acc, inv_l);
+        }
+        a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+            (L > 0.f) ? (M + lg2_approx(L)) * kLn2 : -INFINITY;
+    }
+}
 
 template <class T>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
@@ -639,7 +782,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             const float alpha = aux->mb_alpha[sig_idx<T>(t, j)][r];
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
-                if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((j - 1) & 1), wc,
+                if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, j - 1)]), sig_par<T>(j - 1), wc,
                                kErrWaitTimeout | kSiteCorrPv)) {
                     ok = false;
                     break;
@@ -672,22 +815,42 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         const float l = aux->mb_l[t][r];
         const float m = aux->mb_m[t][r];
         if (nk > 0) {
-            // O is final once PV(nk-1) completed.  A parity wait is exact only
-            // while the barrier is at most one phase behind: with NQ = 2 the
-            // last score MMA waited for PV(nk-2), so one wait suffices; with
-            // NQ = 1 it only waited for PV(nk-3), so PV(nk-2) comes first.
-            if (T::NQ == 1 && nk >= 2 &&
-                !mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((nk - 2) & 1), wc,
-                           kErrWaitTimeout | kSiteEpiPv)) {
-                ok = false;
-                break;
-            }
-            if (!mbar_wait(smem_u32(&aux->bar_pv_done[t]), (uint32_t)((nk - 1) & 1), wc,
+            // O is final once PV(nk-1) completed (value MMAs into one
+            // accumulator complete in issue order).  The wait is exact: the
+            // previous PV on the same barrier copy completed before the last
+            // score MMA was issued.
+            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, nk - 1)]), sig_par<T>(nk - 1), wc,
                            kErrWaitTimeout | kSiteEpiPv)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+        }
+        if (w.piece >= 0) {
+            // a piece of a split unit: unnormalised O, row max and row sum
+            // -> this piece's scratch slot (merged below)
+            float4* po = reinterpret_cast<float4*>(
+                a.part_o + ((size_t)w.piece * T::NQ + t) * (T::D_COLS * T::BM));
+#pragma unroll 1
+            for (int c32 = 0; c32 < T::D_COLS / 32; ++c32) {
+                uint32_t v[32];
+                if (nk > 0) {
+                    tmem_ld32(lane_base + T::o_col(t) + c32 * 32, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    po[(size_t)(c32 * 8 + q) * T::BM + r] =
+                        make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+            float* ml = a.part_ml + ((size_t)w.piece * T::NQ + t) * 2 * T::BM;
+            ml[r] = (nk > 0) ? m : -INFINITY;
+            ml[T::BM + r] = (nk > 0) ? l : 0.f;
+            continue;
         }
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const uint32_t stage = sQ + t * T::QTILE;
@@ -735,6 +898,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
     }
     if (issuer) bulk_wait_group_0();
+    if (ok && w.piece >= 0) tail_merge<T>(a, w, aux, r, wc);
 }
 
 // --------------------------------------------------------------- kernel ----
@@ -767,16 +931,19 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&aux->bar_p_ready[i]), 8);   // 4 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_mb_full[i]), 4);
+            mbar_init(smem_u32(&aux->bar_pv_done[i]), 1);
         }
         for (int t = 0; t < T::NQ; ++t) {
-            mbar_init(smem_u32(&aux->bar_pv_done[t]), 1);
             mbar_init(smem_u32(&aux->bar_fin[t]), 4);
             mbar_init(smem_u32(&aux->bar_epi[t]), 4);
         }
         mbar_init(smem_u32(&aux->bar_drain[0]), 1);
         mbar_init(smem_u32(&aux->bar_drain[1]), 1);
         mbar_init(smem_u32(&aux->bar_tail), 1);
+        mbar_init(smem_u32(&aux->bar_split_a), 4);
+        mbar_init(smem_u32(&aux->bar_split_b), 1);
         aux->abort_flag = 0;
+        aux->merge_last = 0;
         mbar_fence_init();
     }
     if (warp == T::MMA_WARP) {
@@ -788,7 +955,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = aux->tmem_base;
     const WaitCtx wc{&aux->abort_flag, args.err_word, args.wait_limit_ns};
-    const int block_lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+    const int block_lin = blockIdx.x;
     unsigned long long* tr = (args.trace != nullptr && block_lin == args.trace_block) ? args.trace
                                                                                      : nullptr;
 
@@ -823,7 +990,7 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)p.args.num_mblk, (unsigned)p.args.Hq, (unsigned)p.args.B);
+    const unsigned grid = (unsigned)p.args.n_full + (unsigned)p.n_tail * (unsigned)p.args.split;
     kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o, p.args);
     return cudaGetLastError();
 }

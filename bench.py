@@ -49,8 +49,8 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("ef073acfda8b5f3f741aa66a69108e415256c80d577b2e3f4587a97e0180b8f3",
-                114902016, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    "prefill": ("31915540b5bade9598507651c9353eb16e81ca916d98650ad91f05c95a1d8137",
+                118789888, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
     # captured at batch 16 (463.64 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
     "decode": ("ccee9490d466358969a2ce27889455468df8582642f5d88bbe9ebe7b648ca774",

@@ -75,7 +75,12 @@ typedef enum fa_status {
  * value MMA (O += P V) into tensor memory, softmax warpgroups turn S into P
  * with exp2, and a correction/epilogue warpgroup rebases O and writes O and
  * LSE ("b200-flash-attention4-planner", section A1 "Role example" and
- * section E steps 3-8).
+ * section E steps 3-8).  One CTA per query block; for non-causal problems
+ * the query blocks of the last, partial wave are split along the key axis
+ * over several CTAs and merged on the device (see fa_debug_prefill_plan),
+ * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
+ * with cudaFreeAsync on the same stream) of at most SMs * 130 KB (head_dim
+ * 128; in proportion for other head dims).
  * Sizes: batch, hq, hkv, sq, sk >= 0 (any zero size is a no-op returning
  * FA_OK, except sk == 0 with non-empty outputs, which writes O = 0 and
  * LSE = -inf); batch <= 65535, hq <= 65535.
@@ -218,6 +223,20 @@ fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t str
  * slots are left untouched.  buf = NULL switches tracing off.
  */
 fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
+
+/*
+ * The work split fa_fwd_prefill would use for a problem on a device with
+ * `num_sms` SMs, computed on the host (no device needed).  A unit is one
+ * (batch entry, query head, query block of 256 rows for head_dim <= 128, 128
+ * for 256); it visits nk = ceil(sk / 128) key blocks.  The grid's first
+ * out[0] CTAs each process a whole unit; the remaining out[1] units (the last
+ * partial wave) are each processed by out[2] CTAs, piece i taking key blocks
+ * [i nk / out[2], (i + 1) nk / out[2]), and the last piece to finish merges
+ * the pieces' partial results.  Returns FA_ERR_INVALID_ARG for sizes that
+ * fa_fwd_prefill rejects or num_sms < 1.
+ */
+fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                int num_sms, int *out);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 int fa_version(void);

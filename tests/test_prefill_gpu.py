@@ -188,3 +188,53 @@ def test_barrier_protocol_stress(B, Hq, Sq, Sk, d, causal):
     torch.cuda.synchronize()
     check_device_error()
     assert torch.equal(o, o0) and torch.equal(l, l0)
+
+
+SPLIT = [
+    # B, Hq, Hkv, Sq, Sk, d, lengths: non-causal shapes whose query blocks do
+    # not fill whole waves of the GPU, so the last wave's blocks are computed
+    # in pieces along the key axis and merged on the device
+    (1, 1, 1, 16384, 16384, 128, None),     # 64 blocks -> 2 pieces each
+    (1, 2, 2, 5000, 7000, 96, None),        # 40 blocks -> 3 pieces each
+    (1, 2, 2, 3000, 9000, 256, None),       # 48 blocks -> 3 pieces each
+    (3, 1, 1, 2000, 30000, 64, [30000, 0, 17]),   # 24 blocks -> 6 pieces; empty pieces
+    (2, 16, 4, 4096, 4096, 128, None),      # the bench shape with GQA: 56 tail blocks
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,lengths", SPLIT,
+                         ids=[f"b{c[0]}h{c[1]}x{c[2]}q{c[3]}k{c[4]}d{c[5]}" for c in SPLIT])
+def test_split_units_sampled_rows(B, Hq, Hkv, Sq, Sk, d, lengths):
+    """Query blocks computed in pieces by several CTAs and merged by the last
+    piece to finish: sampled rows (tile edges of a few heads plus random rows)
+    against the oracle, finiteness of every output row that sees a key."""
+    from attention_forward_blackwell_gb300 import inputs
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=500 + Sq % 97, device="cuda",
+                           lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(x, scale, False)
+    lens = [Sk] * B if lengths is None else lengths
+    for b in range(B):
+        if lens[b] > 0:
+            assert torch.isfinite(o[b]).all() and torch.isfinite(lse[b]).all()
+        else:
+            assert torch.all(o[b] == 0) and torch.all(torch.isneginf(lse[b]))
+    rows = sample_rows(B, Hq, Sq, n_random=192, seed=Sq)
+    ro, rl = oracle_for(x, scale, False, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, f"split {B, Hq, Hkv, Sq, Sk, d}")
+    del x, o, lse
+    free_cuda()
+
+
+def test_split_units_are_deterministic():
+    """The merge of split units does not depend on which piece arrives last."""
+    from attention_forward_blackwell_gb300 import inputs
+    x = inputs.make_inputs(1, 1, 1, 16384, 16384, 128, tag=503, device="cuda")
+    o1, l1 = _run(x, 0.088, False)
+    for _ in range(5):
+        o2, l2 = _run(x, 0.088, False)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
