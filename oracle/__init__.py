@@ -60,6 +60,10 @@ def _load(lib_path=None):
                 fn.restype = ctypes.c_int
                 fn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i64, vp,
                                dbl, ctypes.c_int, vp, i64, vp, vp]
+            ex = lib.oracle_attention_fwd_ex
+            ex.restype = ctypes.c_int
+            ex.argtypes = [vp, vp, vp, ctypes.c_int, i64, i64, i64, i64, i64, i64, vp,
+                           dbl, ctypes.c_int, i64, vp, vp, i64, vp, vp]
             _libs[key] = lib
     return _libs[key]
 
@@ -69,7 +73,7 @@ def _ptr(a):
 
 
 def attention_fwd(q, k, v, *, scale, causal=False, seqlens_k=None, rows=None,
-                  threads=1, lib_path=None):
+                  threads=1, lib_path=None, window=0, sinks=None):
     """Masked softmax attention with per-row LSE, in fp64.
 
     q: [B, Hq, Sq, d]; k, v: [B, Hkv, Sk, d].  All three are either ``uint16``
@@ -83,6 +87,9 @@ def attention_fwd(q, k, v, *, scale, causal=False, seqlens_k=None, rows=None,
     same single-threaded C routine (each call computes disjoint rows).
     ``lib_path`` loads a different build of ``oracle.c`` (the oracle's own
     mutation test uses it to check that its pins catch planted mistakes).
+    ``window`` > 0 keeps, for row i, only keys j > i + (L - Sq) - window;
+    ``sinks``: optional Hq sink logits (units of the scaled score) that join
+    each row's softmax normaliser without a value (see oracle.c).
     """
     lib = _load(lib_path)
     q = np.ascontiguousarray(q)
@@ -91,9 +98,9 @@ def attention_fwd(q, k, v, *, scale, causal=False, seqlens_k=None, rows=None,
     if not (q.dtype == k.dtype == v.dtype):
         raise TypeError("q, k, v must share one dtype")
     if q.dtype == np.uint16:
-        fn = lib.oracle_attention_fwd_bf16
+        fn, kind = lib.oracle_attention_fwd_bf16, 0
     elif q.dtype == np.float64:
-        fn = lib.oracle_attention_fwd_f64
+        fn, kind = lib.oracle_attention_fwd_f64, 1
     else:
         raise TypeError(f"unsupported dtype {q.dtype}")
     B, Hq, Sq, d = q.shape
@@ -105,6 +112,12 @@ def attention_fwd(q, k, v, *, scale, causal=False, seqlens_k=None, rows=None,
         sl = np.ascontiguousarray(np.asarray(seqlens_k, dtype=np.int32))
         if sl.shape != (B,):
             raise ValueError("seqlens_k must have B entries")
+    sk_arr = None
+    if sinks is not None:
+        sk_arr = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64))
+        if sk_arr.shape != (q.shape[1],):
+            raise ValueError("sinks must have Hq entries")
+    extended = int(window) > 0 or sk_arr is not None
     full = rows is None
     if full:
         rows = np.arange(B * Hq * Sq, dtype=np.int64)
@@ -119,6 +132,11 @@ def attention_fwd(q, k, v, *, scale, causal=False, seqlens_k=None, rows=None,
         r = rows[lo:hi]
         o_part = o[lo:hi]
         l_part = lse[lo:hi]
+        if extended:
+            return lib.oracle_attention_fwd_ex(
+                _ptr(q), _ptr(k), _ptr(v), kind, B, Hq, Hkv, Sq, Sk, d, _ptr(sl),
+                float(scale), int(bool(causal)), int(window), _ptr(sk_arr), _ptr(r),
+                hi - lo, _ptr(o_part), _ptr(l_part))
         return fn(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, Sq, Sk, d, _ptr(sl),
                   float(scale), int(bool(causal)), _ptr(r), hi - lo,
                   _ptr(o_part), _ptr(l_part))

@@ -39,6 +39,17 @@
  *     E.2 asks that the exp basis be stated; the GPU may use exp2 internally
  *     but reports this quantity).
  *   - Inputs are bf16 bit patterns (decoded exactly to double) or doubles.
+ *   - Sliding window ("2026-05-28_STATUS.md", items D3 "SWA length mask" and
+ *     D4 "causal mask on SWA"): with window W > 0, key j is visible to row i
+ *     only if j > p_i - W, where p_i = i + (L - Sq) is the row's aligned key
+ *     position; with causal this keeps the row's own key and the W - 1 keys
+ *     before it.  W <= 0 means no window.
+ *   - Attention sink (same page, item D5c "sink merge": one softmax over the
+ *     scores and the sink): an optional per-query-head logit sigma_h in the
+ *     units of the scaled score joins the softmax's normaliser but carries no
+ *     value, so O_i = sum_j e^{s_j} v_j / (e^{sigma_h} + sum_j e^{s_j}) and
+ *     LSE_i = ln(e^{sigma_h} + sum_j e^{s_j}); a row with no visible key then
+ *     has O = 0 and LSE = sigma_h.
  */
 #include <math.h>
 #include <stdint.h>
@@ -66,7 +77,8 @@ static double oracle_load(const void *base, int kind, int64_t index)
 static void oracle_one_row(const void *q, const void *k, const void *v, int kind,
                            int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq,
                            int64_t Sk, int64_t d, const int32_t *seqlens_k,
-                           double scale, int causal, int64_t r,
+                           double scale, int causal, int64_t window,
+                           const double *sinks, int64_t r,
                            double *scores, double *o_row, double *lse_out)
 {
     int64_t i = r % Sq;
@@ -75,7 +87,8 @@ static void oracle_one_row(const void *q, const void *k, const void *v, int kind
     int64_t group = Hq / Hkv;          /* query heads per key/value head */
     int64_t hk = h / group;            /* key/value head read by query head h */
     int64_t L = Sk;                    /* valid keys of batch entry b */
-    int64_t last, n, j, c;
+    int64_t first, last, n, j, c;
+    double sink = -INFINITY;           /* sink logit of head h (none: -inf) */
     const int64_t q_off = ((b * Hq + h) * Sq + i) * d;
     const int64_t kv_head_off = (b * Hkv + hk) * Sk * d;
     double m, l;
@@ -86,21 +99,27 @@ static void oracle_one_row(const void *q, const void *k, const void *v, int kind
         if (L < 0) L = 0;
         if (L > Sk) L = Sk;
     }
+    if (sinks != NULL)
+        sink = sinks[h];
     last = L - 1;                      /* last visible key */
     if (causal && i + (L - Sq) < last)
         last = i + (L - Sq);
-    n = last + 1;                      /* visible keys are j = 0 .. n-1 */
+    first = 0;                         /* first visible key */
+    if (window > 0 && i + (L - Sq) - window + 1 > first)
+        first = i + (L - Sq) - window + 1;
+    n = last + 1;                      /* visible keys are j = first .. n-1 */
 
     for (c = 0; c < d; ++c)
         o_row[c] = 0.0;
-    if (n <= 0) {                      /* no visible key */
-        *lse_out = -INFINITY;
+    if (n <= first) {                  /* no visible key */
+        *lse_out = sink;               /* -inf without a sink */
         return;
     }
 
-    /* pass 1: scaled scores s_j = scale * sum_c q[c] k_j[c], and their max */
-    m = -INFINITY;
-    for (j = 0; j < n; ++j) {
+    /* pass 1: scaled scores s_j = scale * sum_c q[c] k_j[c], and their max
+       (the sink logit counts as one more score) */
+    m = sink;
+    for (j = first; j < n; ++j) {
         double dot = 0.0;
         for (c = 0; c < d; ++c)
             dot += oracle_load(q, kind, q_off + c) *
@@ -110,9 +129,10 @@ static void oracle_one_row(const void *q, const void *k, const void *v, int kind
             m = scores[j];
     }
 
-    /* pass 2: weights exp(s_j - m), their sum l, and sum_j weight_j * v_j */
-    l = 0.0;
-    for (j = 0; j < n; ++j) {
+    /* pass 2: weights exp(s_j - m), their sum l (with the sink's weight, which
+       multiplies no value row), and sum_j weight_j * v_j */
+    l = (sinks != NULL) ? exp(sink - m) : 0.0;
+    for (j = first; j < n; ++j) {
         double w = exp(scores[j] - m);
         l += w;
         for (c = 0; c < d; ++c)
@@ -133,7 +153,8 @@ static void oracle_one_row(const void *q, const void *k, const void *v, int kind
 static int oracle_rows(const void *q, const void *k, const void *v, int kind,
                        int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq,
                        int64_t Sk, int64_t d, const int32_t *seqlens_k,
-                       double scale, int causal, const int64_t *rows,
+                       double scale, int causal, int64_t window,
+                       const double *sinks, const int64_t *rows,
                        int64_t n_rows, double *o_out, double *lse_out)
 {
     int64_t t, total;
@@ -150,7 +171,7 @@ static int oracle_rows(const void *q, const void *k, const void *v, int kind,
         int64_t r = rows ? rows[t] : t;
         if (r < 0 || r >= total) { free(scores); return -1; }
         oracle_one_row(q, k, v, kind, B, Hq, Hkv, Sq, Sk, d, seqlens_k, scale,
-                       causal, r, scores, o_out + t * d, lse_out + t);
+                       causal, window, sinks, r, scores, o_out + t * d, lse_out + t);
     }
     free(scores);
     return 0;
@@ -165,7 +186,7 @@ int oracle_attention_fwd_bf16(const uint16_t *q, const uint16_t *k,
                               double *o_out, double *lse_out)
 {
     return oracle_rows(q, k, v, 0, B, Hq, Hkv, Sq, Sk, d, seqlens_k, scale,
-                       causal, rows, n_rows, o_out, lse_out);
+                       causal, 0, NULL, rows, n_rows, o_out, lse_out);
 }
 
 /* Inputs as doubles (used by the closed-form checks of the oracle itself). */
@@ -176,5 +197,20 @@ int oracle_attention_fwd_f64(const double *q, const double *k, const double *v,
                              int64_t n_rows, double *o_out, double *lse_out)
 {
     return oracle_rows(q, k, v, 1, B, Hq, Hkv, Sq, Sk, d, seqlens_k, scale,
-                       causal, rows, n_rows, o_out, lse_out);
+                       causal, 0, NULL, rows, n_rows, o_out, lse_out);
+}
+
+/* Same, with a sliding window (window <= 0: none) and per-query-head sink
+   logits (sinks: Hq doubles, or NULL for none); kind 0 = bf16 bits,
+   1 = doubles. */
+int oracle_attention_fwd_ex(const void *q, const void *k, const void *v, int kind,
+                            int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq,
+                            int64_t Sk, int64_t d, const int32_t *seqlens_k,
+                            double scale, int causal, int64_t window,
+                            const double *sinks, const int64_t *rows,
+                            int64_t n_rows, double *o_out, double *lse_out)
+{
+    if (kind != 0 && kind != 1) return -1;
+    return oracle_rows(q, k, v, kind, B, Hq, Hkv, Sq, Sk, d, seqlens_k, scale,
+                       causal, window, sinks, rows, n_rows, o_out, lse_out);
 }

@@ -321,7 +321,122 @@ def pin_row_subset(attn):
     _close(ls_, lse.reshape(-1)[rows], 0, "subset LSE")
 
 
+# ------------------------------------------- sliding window and sinks ----
+# Readings: "2026-05-28_STATUS.md" items D3/D4 (window mask, with causal) and
+# D5c (one softmax over the scores and the sink); see oracle.c.
+
+
+def pin_window_covering_all_keys(attn):
+    """A window wider than every row's key range changes nothing (exactly)."""
+    rng = np.random.default_rng(21)
+    B, Hq, Hkv, Sq, Sk, d = 2, 2, 1, 7, 9, 3
+    q, k, v = (_rand(rng, s) for s in ((B, Hq, Sq, d), (B, Hkv, Sk, d), (B, Hkv, Sk, d)))
+    for causal in (False, True):
+        o0, l0 = attn(q, k, v, scale=0.7, causal=causal, seqlens_k=[9, 5])
+        o1, l1 = attn(q, k, v, scale=0.7, causal=causal, seqlens_k=[9, 5], window=Sk + Sq)
+        _close(o1, o0, 0, "wide window O")
+        _close(l1, l0, 0, "wide window LSE")
+
+
+def pin_window_one_is_own_key(attn):
+    """Causal with a window of one key: row i sees only key p = i + L - Sq, so
+    O_i = v_p and LSE_i = scale q_i . k_p; rows with p < 0 see nothing."""
+    rng = np.random.default_rng(22)
+    B, Hq, Hkv, Sq, Sk, d = 2, 2, 2, 6, 6, 4
+    q, k, v = (_rand(rng, s) for s in ((B, Hq, Sq, d), (B, Hkv, Sk, d), (B, Hkv, Sk, d)))
+    lens = [6, 3]
+    o, lse = attn(q, k, v, scale=0.3, causal=True, seqlens_k=lens, window=1)
+    for b in range(B):
+        for h in range(Hq):
+            for i in range(Sq):
+                p = i + lens[b] - Sq
+                if p < 0:
+                    _close(o[b, h, i], np.zeros(d), 0, "empty row O")
+                    assert lse[b, h, i] == -math.inf, "empty row LSE"
+                else:
+                    _close(o[b, h, i], v[b, h, p], 1e-15, "own-key O")
+                    _close(lse[b, h, i], 0.3 * float(np.dot(q[b, h, i], k[b, h, p])), 1e-14,
+                           "own-key LSE")
+
+
+def pin_window_equals_sliced_keys(attn):
+    """Row i with window W sees keys [p - W + 1, p] (causal) or [p - W + 1, L)
+    (not causal), p = i + L - Sq: the same as the unwindowed definition on K, V
+    sliced to those keys, for that row alone."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, Sq, Sk, d = 1, 2, 1, 5, 12, 3
+    q, k, v = (_rand(rng, s) for s in ((B, Hq, Sq, d), (B, Hkv, Sk, d), (B, Hkv, Sk, d)))
+    L, W = 10, 4
+    for causal in (False, True):
+        o, lse = attn(q, k, v, scale=0.9, causal=causal, seqlens_k=[L], window=W)
+        for i in range(Sq):
+            p = i + L - Sq
+            lo, hi = max(0, p - W + 1), (p + 1 if causal else L)
+            ks, vs = k[:, :, lo:hi], v[:, :, lo:hi]
+            o1, l1 = attn(q[:, :, i:i + 1], np.ascontiguousarray(ks), np.ascontiguousarray(vs),
+                          scale=0.9)
+            _close(o[:, :, i], o1[:, :, 0], 1e-14, f"sliced window O row {i}")
+            _close(lse[:, :, i], l1[:, :, 0], 1e-14, f"sliced window LSE row {i}")
+
+
+def pin_sink_zero_query(attn):
+    """Q = 0: every score is 0, so O = sum_j v_j / (e^sigma + n) and
+    LSE = ln(e^sigma + n) (n visible keys)."""
+    rng = np.random.default_rng(24)
+    B, Hq, Hkv, Sq, Sk, d = 1, 3, 1, 2, 5, 3
+    q = np.zeros((B, Hq, Sq, d))
+    k, v = _rand(rng, (B, Hkv, Sk, d)), _rand(rng, (B, Hkv, Sk, d))
+    sig = np.array([-2.0, 0.5, 3.0])
+    o, lse = attn(q, k, v, scale=1.0, sinks=sig)
+    for h in range(Hq):
+        den = math.exp(sig[h]) + Sk
+        _close(o[0, h], np.broadcast_to(v[0, 0].sum(axis=0) / den, (Sq, d)), 1e-15, "sink O")
+        _close(lse[0, h], np.full(Sq, math.log(den)), 1e-15, "sink LSE")
+
+
+def pin_sink_is_a_zero_value_key(attn):
+    """A sink equals one more key whose score is exactly sigma and whose value
+    row is zero."""
+    rng = np.random.default_rng(25)
+    B, H, Sq, Sk, d = 1, 2, 1, 6, 4
+    q = _rand(rng, (B, H, Sq, d), 0.5, 1.0)
+    k, v = _rand(rng, (B, H, Sk, d)), _rand(rng, (B, H, Sk, d))
+    sig = np.array([0.75, -1.25])
+    scale = 0.5
+    k2 = np.concatenate([k, np.zeros((B, H, 1, d))], axis=2)
+    v2 = np.concatenate([v, np.zeros((B, H, 1, d))], axis=2)
+    for h in range(H):
+        k2[0, h, Sk, 0] = sig[h] / (scale * q[0, h, 0, 0])   # score = sigma (to rounding)
+    o, lse = attn(q, k, v, scale=scale, sinks=sig)
+    o2, l2 = attn(q, k2, v2, scale=scale)
+    _close(o, o2, 1e-14, "sink as a key O")
+    _close(lse, l2, 1e-14, "sink as a key LSE")
+
+
+def pin_sink_extremes(attn):
+    """sigma = -inf is no sink (exactly); sigma = 1000 takes all the weight
+    (O = 0, LSE = 1000); a row without keys has LSE = sigma."""
+    rng = np.random.default_rng(26)
+    B, Hq, Hkv, Sq, Sk, d = 2, 2, 1, 4, 4, 3
+    q, k, v = (_rand(rng, s) for s in ((B, Hq, Sq, d), (B, Hkv, Sk, d), (B, Hkv, Sk, d)))
+    o0, l0 = attn(q, k, v, scale=0.8, causal=True, seqlens_k=[4, 2])
+    o1, l1 = attn(q, k, v, scale=0.8, causal=True, seqlens_k=[4, 2],
+                  sinks=[-math.inf, -math.inf])
+    _close(o1, o0, 0, "-inf sink O")
+    _close(l1, l0, 0, "-inf sink LSE")
+    o2, l2 = attn(q, k, v, scale=0.8, causal=True, seqlens_k=[4, 2], sinks=[1000.0, 1000.0])
+    _close(o2, np.zeros_like(o2), 1e-300, "huge sink O")
+    _close(l2, np.full_like(l2, 1000.0), 1e-12, "huge sink LSE")
+    o3, l3 = attn(q, k, v, scale=0.8, causal=True, seqlens_k=[4, 2], sinks=[0.25, -0.5])
+    # batch entry 1 has L = 2 < Sq = 4: rows 0 and 1 see no key
+    _close(o3[1, :, :2], np.zeros((Hq, 2, d)), 0, "sink empty-row O")
+    _close(l3[1, :, :2], np.array([[0.25, 0.25], [-0.5, -0.5]]), 0, "sink empty-row LSE")
+
+
 ALL_PINS = [pin_golden_closed_forms, pin_zero_query_gives_mean_of_values,
             pin_single_key, pin_causal_first_row, pin_shift_invariance,
             pin_bruteforce_tiny, pin_library_sdpa, pin_permutation_invariance,
-            pin_gqa_equals_repeated_heads, pin_bf16_decoding, pin_row_subset]
+            pin_gqa_equals_repeated_heads, pin_bf16_decoding, pin_row_subset,
+            pin_window_covering_all_keys, pin_window_one_is_own_key,
+            pin_window_equals_sliced_keys, pin_sink_zero_query,
+            pin_sink_is_a_zero_value_key, pin_sink_extremes]

@@ -28,6 +28,14 @@ MUTATIONS = [
      "uint32_t word = ((uint32_t)bits) << 15;"),
     ("max_not_subtracted_in_weights", "double w = exp(scores[j] - m);",
      "double w = exp(scores[j]);"),
+    ("window_off_by_one", "first = i + (L - Sq) - window + 1;",
+     "first = i + (L - Sq) - window;"),
+    ("window_ignored", "if (window > 0 && i + (L - Sq) - window + 1 > first)",
+     "if (0 && i + (L - Sq) - window + 1 > first)"),
+    ("sink_weight_dropped", "l = (sinks != NULL) ? exp(sink - m) : 0.0;", "l = 0.0;"),
+    ("sink_not_in_max", "    m = sink;\n", "    m = -INFINITY;\n"),
+    ("empty_row_ignores_sink", "*lse_out = sink;               /* -inf without a sink */",
+     "*lse_out = -INFINITY;"),
 ]
 
 
