@@ -26,6 +26,12 @@ _VP, _I, _F, _LL = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longl
 _FWD = [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP, _I, _F, _I]
 SIGNATURES = {
     "fa_fwd_prefill": (_I, _FWD + [_VP]),
+    "fa_fwd_prefill_ex": (_I, _FWD + [_I, _VP, _VP]),
+    "fa_fwd_decode_ex": (_I, _FWD + [_I, _VP, _VP]),
+    "fa_fwd_prefill_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _I, _I,
+                                  _I, _F, _I, _VP]),
+    "fa_fwd_decode_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _I, _I,
+                                 _I, _F, _I, _VP]),
     "fa_fwd_decode": (_I, _FWD + [_VP]),
     "fa_fwd_decode_splits": (_I, _FWD + [_I, _VP]),
     "fa_fwd_decode_noalloc": (_I, _FWD + [_VP]),
@@ -119,36 +125,98 @@ def _outputs(q, out, lse):
     return out, lse
 
 
+def _check_sinks(sinks, q):
+    if sinks is None:
+        return None
+    if sinks.dtype != torch.float32 or sinks.shape != (q.shape[1],) or not sinks.is_cuda:
+        raise ValueError("sinks must be a CUDA fp32 tensor of shape [Hq]")
+    return sinks.contiguous()
+
+
 def prefill(q, k, v, scale=None, causal=False, seqlens_k=None, out=None, lse=None,
-            stream=None):
-    """Attention forward through ``fa_fwd_prefill``; returns (o, lse)."""
+            stream=None, window=0, sinks=None):
+    """Attention forward through ``fa_fwd_prefill`` (``fa_fwd_prefill_ex`` with
+    a sliding ``window`` > 0 or per-head ``sinks``); returns (o, lse)."""
     B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
     out, lse = _outputs(q, out, lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    st = lib().fa_fwd_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
-                              Sq, Sk, _ptr(seqlens_k), d, scale, int(bool(causal)),
-                              _stream_ptr(stream))
+    sinks = _check_sinks(sinks, q)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk,
+            _ptr(seqlens_k), d, scale, int(bool(causal)))
+    if (window and window > 0) or sinks is not None:
+        st = lib().fa_fwd_prefill_ex(*args, int(window or 0), _ptr(sinks), _stream_ptr(stream))
+    else:
+        st = lib().fa_fwd_prefill(*args, _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_prefill")
     return out, lse
 
 
 def decode(q, k, v, scale=None, causal=False, seqlens_k=None, num_splits=0, out=None,
-           lse=None, stream=None):
+           lse=None, stream=None, window=0, sinks=None):
     """Split-KV attention forward through ``fa_fwd_decode_splits``
-    (num_splits <= 0 lets the library choose, as ``fa_fwd_decode`` does)."""
+    (num_splits <= 0 lets the library choose, as ``fa_fwd_decode`` does), or
+    ``fa_fwd_decode_ex`` with a sliding ``window`` > 0 or per-head ``sinks``."""
     B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
     out, lse = _outputs(q, out, lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    sinks = _check_sinks(sinks, q)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk,
             _ptr(seqlens_k), d, scale, int(bool(causal)))
-    if num_splits and num_splits > 0:
+    if (window and window > 0) or sinks is not None:
+        if num_splits and num_splits > 0:
+            raise ValueError("num_splits cannot be combined with window or sinks")
+        st = lib().fa_fwd_decode_ex(*args, int(window or 0), _ptr(sinks), _stream_ptr(stream))
+    elif num_splits and num_splits > 0:
         st = lib().fa_fwd_decode_splits(*args, int(num_splits), _stream_ptr(stream))
     else:
         st = lib().fa_fwd_decode(*args, _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_decode")
     return out, lse
+
+
+def _paged(name, q, k_cache, v_cache, block_table, seqlens_k, scale, causal, out, lse, stream):
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda):
+        raise ValueError("q and the caches must be CUDA tensors")
+    if q.dtype != torch.bfloat16 or k_cache.dtype != torch.bfloat16 or v_cache.dtype != torch.bfloat16:
+        raise ValueError("q and the caches must be bf16")
+    if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
+        raise ValueError("caches must share a shape [num_pages, Hkv, page_size, d]")
+    B, Hq, Sq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_cache.shape
+    if dk != d:
+        raise ValueError("head dims differ")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    if seqlens_k is None or seqlens_k.dtype != torch.int32 or seqlens_k.shape != (B,):
+        raise ValueError("seqlens_k must be int32 [B]")
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    block_table, seqlens_k = block_table.contiguous(), seqlens_k.contiguous()
+    out, lse = _outputs(q, out, lse)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = getattr(lib(), name)(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), B, Hq,
+                              Hkv, Sq, _ptr(seqlens_k), _ptr(block_table), block_table.shape[1],
+                              page_size, num_pages, d, scale, int(bool(causal)),
+                              _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, name)
+    return out, lse
+
+
+def prefill_paged(q, k_cache, v_cache, block_table, seqlens_k, scale=None, causal=False,
+                  out=None, lse=None, stream=None):
+    """Prefill over paged caches [num_pages, Hkv, page_size, d] through
+    ``fa_fwd_prefill_paged`` (page_size a multiple of 128); returns (o, lse)."""
+    return _paged("fa_fwd_prefill_paged", q, k_cache, v_cache, block_table, seqlens_k, scale,
+                  causal, out, lse, stream)
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, scale=None, causal=False,
+                 out=None, lse=None, stream=None):
+    """Decode over paged caches through ``fa_fwd_decode_paged``; returns (o, lse)."""
+    return _paged("fa_fwd_decode_paged", q, k_cache, v_cache, block_table, seqlens_k, scale,
+                  causal, out, lse, stream)
 
 
 def get_device_error(stream=None) -> int:

@@ -127,12 +127,28 @@ fa_status check_common(const void* q, const void* k, const void* v, void* o, flo
 
 fa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? FA_OK : FA_ERR_CUDA; }
 
+// Checks of the paged-cache arguments shared by prefill and decode.
+fa_status check_paged(const int* seqlens_k, const int* block_table, int max_pages, int page_size,
+                      int num_pages, int batch, int hq, int sq) {
+    if (batch == 0 || hq == 0 || sq == 0) return FA_OK;   // nothing to compute
+    if (!seqlens_k || !block_table) return FA_ERR_INVALID_ARG;
+    if (max_pages <= 0 || page_size <= 0 || num_pages <= 0) return FA_ERR_INVALID_ARG;
+    if ((long long)max_pages * page_size >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(block_table) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) != 0)
+        return FA_ERR_MISALIGNED;
+    return FA_OK;
+}
+
 fa_status decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
-                      float scale, int causal, int num_splits, fa_stream_t stream) {
+                      float scale, int causal, int window, const float* sinks, int num_splits,
+                      fa_stream_t stream, const int* block_table = nullptr, int max_pages = 0,
+                      int page_size = 0, int num_pages = 0) {
     Common c;
     fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
     if (st != FA_OK || c.noop) return st;
+    if ((reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return FA_ERR_MISALIGNED;
     if (sq > FA_DECODE_MAX_SQ) return FA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return FA_ERR_UNSUPPORTED;
     const long long q_elems = (long long)batch * hq * sq * head_dim;
@@ -143,7 +159,8 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (sk == 0)
         return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
-                                           (long long)batch * hq * sq, head_dim, s));
+                                           (long long)batch * hq * sq, head_dim, sinks, hq, sq,
+                                           s));
 
     DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);
@@ -161,6 +178,12 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     a.rows = a.group * sq;
     a.n_mtiles = (a.rows + 15) / 16;
     a.causal = causal ? 1 : 0;
+    a.window = window > 0 ? window : 0;
+    a.sinks = sinks;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
     a.scale_log2 = scale * 1.4426950408889634f;
     if ((long long)hkv * a.n_mtiles > 65535) return FA_ERR_INVALID_ARG;
     // split planning: equal chunks of a multiple of 64 keys
@@ -191,19 +214,17 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     return FA_OK;
 }
 
-}  // namespace
-}  // namespace fa
-
-using namespace fa;
-
-extern "C" {
-
-fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
-                         int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
-                         int head_dim, float scale, int causal, fa_stream_t stream) {
+// Prefill on contiguous K/V (block_table == nullptr) or on paged caches
+// [num_pages, hkv, page_size, d] (sk = max_pages * page_size keys per sequence).
+fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
+                       float scale, int causal, int window, const float* sinks,
+                       const int* block_table, int max_pages, int page_size, int num_pages,
+                       fa_stream_t stream) {
     Common c;
     fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
     if (st != FA_OK || c.noop) return st;
+    if ((reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return FA_ERR_MISALIGNED;
     if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
         return FA_ERR_UNSUPPORTED;
     const DeviceInfo* di = device_info();
@@ -212,11 +233,14 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (sk == 0)
         return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
-                                           (long long)batch * hq * sq, head_dim, s));
+                                           (long long)batch * hq * sq, head_dim, sinks, hq, sq,
+                                           s));
     PrefillLaunch p;
+    const int kv_rows = block_table ? page_size : sk;
+    const long long kv_planes = block_table ? (long long)num_pages * hkv : (long long)batch * hkv;
     if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
-        !encode_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv) ||
-        !encode_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv) ||
+        !encode_map(&p.tm_k, k, head_dim, kv_rows, kv_planes) ||
+        !encode_map(&p.tm_v, v, head_dim, kv_rows, kv_planes) ||
         !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
         return FA_ERR_INVALID_ARG;
     PrefillArgs& a = p.args;
@@ -234,6 +258,11 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     a.num_mblk = (sq + rows_per_cta - 1) / rows_per_cta;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_limit_ns = kWaitLimitNs;
+    a.window = window > 0 ? window : 0;
+    a.sinks = sinks;
+    a.block_table = block_table;
+    a.max_pages = max_pages;
+    a.page_size = page_size;
     a.trace = g_trace_buf;
     a.trace_block = g_trace_block;
     p.head_dim = head_dim;
@@ -242,7 +271,8 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     const long long units = (long long)batch * hq * a.num_mblk;
     if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
     a.nk = (sk + 127) / 128;
-    const PrefillPlan plan = plan_prefill(units, a.nk, p.causal, di->num_sms);
+    // (a windowed unit has fewer key blocks than nk: it is not split either)
+    const PrefillPlan plan = plan_prefill(units, a.nk, p.causal || a.window > 0, di->num_sms);
     a.n_full = plan.n_full;
     a.split = plan.split;
     p.n_tail = plan.n_tail;
@@ -271,11 +301,68 @@ fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, f
     return from_cuda(e);
 }
 
+}  // namespace
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                            int head_dim, float scale, int causal, int window,
+                            const float* sinks, fa_stream_t stream) {
+    return prefill_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                        causal, window, sinks, nullptr, 0, 0, 0, stream);
+}
+
+fa_status fa_fwd_prefill(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                         int head_dim, float scale, int causal, fa_stream_t stream) {
+    return prefill_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                        causal, 0, nullptr, nullptr, 0, 0, 0, stream);
+}
+
+fa_status fa_fwd_prefill_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                               float* lse, int batch, int hq, int hkv, int sq,
+                               const int* seqlens_k, const int* block_table, int max_pages,
+                               int page_size, int num_pages, int head_dim, float scale,
+                               int causal, fa_stream_t stream) {
+    fa_status st = check_paged(seqlens_k, block_table, max_pages, page_size, num_pages, batch, hq,
+                               sq);
+    if (st != FA_OK) return st;
+    if (page_size % 128 != 0) return FA_ERR_UNSUPPORTED;   // a key tile must fit a page
+    return prefill_impl(q, k_cache, v_cache, o, lse, batch, hq, hkv, sq, max_pages * page_size,
+                        seqlens_k, head_dim, scale, causal, 0, nullptr, block_table, max_pages,
+                        page_size, num_pages, stream);
+}
+
 fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,
                         int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
                         int head_dim, float scale, int causal, fa_stream_t stream) {
     return decode_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
-                       causal, 0, stream);
+                       causal, 0, nullptr, 0, stream);
+}
+
+fa_status fa_fwd_decode_ex(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int batch, int hq, int hkv, int sq, int sk, const int* seqlens_k,
+                           int head_dim, float scale, int causal, int window, const float* sinks,
+                           fa_stream_t stream) {
+    return decode_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                       causal, window, sinks, 0, stream);
+}
+
+fa_status fa_fwd_decode_paged(const void* q, const void* k_cache, const void* v_cache, void* o,
+                              float* lse, int batch, int hq, int hkv, int sq,
+                              const int* seqlens_k, const int* block_table, int max_pages,
+                              int page_size, int num_pages, int head_dim, float scale, int causal,
+                              fa_stream_t stream) {
+    fa_status st = check_paged(seqlens_k, block_table, max_pages, page_size, num_pages, batch, hq,
+                               sq);
+    if (st != FA_OK) return st;
+    return decode_impl(q, k_cache, v_cache, o, lse, batch, hq, hkv, sq, max_pages * page_size,
+                       seqlens_k, head_dim, scale, causal, 0, nullptr, 0, stream, block_table,
+                       max_pages, page_size, num_pages);
 }
 
 fa_status fa_fwd_decode_splits(const void* q, const void* k, const void* v, void* o, float* lse,
@@ -283,7 +370,7 @@ fa_status fa_fwd_decode_splits(const void* q, const void* k, const void* v, void
                                int head_dim, float scale, int causal, int num_splits,
                                fa_stream_t stream) {
     return decode_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
-                       causal, num_splits, stream);
+                       causal, 0, nullptr, num_splits, stream);
 }
 
 const char* fa_status_string(fa_status status) {

@@ -25,6 +25,16 @@ struct PrefillArgs {
     unsigned int* err_word;     // device error word
     int B, Hq, Hkv, Sq, Sk;
     int group;                  // Hq / Hkv
+    int window;                 // sliding window in keys (<= 0: none)
+    const float* sinks;         // [Hq] sink logits (scaled-score units) or nullptr
+    // Paged K/V (nullptr: contiguous [B, Hkv, Sk, d]): the caches are
+    // [num_pages, Hkv, page_size, d] and key j of sequence b is row
+    // j % page_size of page block_table[b * max_pages + j / page_size];
+    // page_size is a multiple of the 128-key tile, so a tile never crosses a
+    // page.
+    const int* block_table;
+    int max_pages;
+    int page_size;
     int num_mblk;               // query blocks (units) per (b, h)
     // Work split (see prefill_work): CTAs [0, n_full) process whole units;
     // each later unit is split into `split` pieces of its nk key blocks.
@@ -118,14 +128,24 @@ struct DecodeArgs {
     int n_splits;
     int chunk;                  // keys per split (multiple of 64)
     int causal;
+    int window;                 // sliding window in keys (<= 0: none)
+    const float* sinks;         // [Hq] sink logits (scaled-score units) or nullptr
+    // Paged K/V (nullptr: contiguous): caches [num_pages, Hkv, page_size, d],
+    // key j of sequence b at row j % page_size of page
+    // block_table[b * max_pages + j / page_size] (clamped to the cache).
+    const int* block_table;
+    int max_pages;
+    int page_size;
+    int num_pages;
     float scale_log2;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, int head_dim, cudaStream_t s);
 
-// Fills O = 0 and LSE = -inf (used when there are no keys at all).
+// Fills O = 0 and LSE = -inf, or the row's sink logit when sinks is not null
+// (used when there are no keys at all); rows are ordered (b, h < hq, i < sq).
 cudaError_t launch_fill_empty(uint16_t* o, float* lse, long long rows, int head_dim,
-                              cudaStream_t s);
+                              const float* sinks, int hq, int sq, cudaStream_t s);
 
 // Self-tests of the tcgen05 building blocks (selftest.cu).
 cudaError_t launch_selftest_tmem_roundtrip(const float* in, float* out, cudaStream_t s);

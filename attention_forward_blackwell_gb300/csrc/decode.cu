@@ -29,6 +29,7 @@ namespace fa {
 namespace {
 
 constexpr float kLn2f = 0.69314718055994530942f;
+constexpr float kLog2ef = 1.44269504088896340736f;
 constexpr float kRebase = 8.0f;   // lazy rebase threshold, log2 units
 
 template <int D>
@@ -54,7 +55,7 @@ __device__ __forceinline__ uint32_t swz(int key, int g) {
     return (uint32_t)(key * DecodeTraits<D>::ROW + ((g ^ (key & 7)) << 4));
 }
 
-template <int D>
+template <int D, bool PAGED>
 __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
     decode_split_kernel(const DecodeArgs a) {
     using T = DecodeTraits<D>;
@@ -104,18 +105,35 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
             qa[kk][2 + hrow] = hi;    // a2 / a3
         }
     }
-    // last visible key per fragment row (bottom-right causal alignment)
-    int lim[2];
+    // last and first visible key per fragment row (bottom-right causal
+    // alignment; sliding window)
+    int lim[2], lo[2];
+    int lo_min = 0x7fffffff;
 #pragma unroll
     for (int hrow = 0; hrow < 2; ++hrow) {
         lim[hrow] = k_hi - 1;
         if (a.causal && qi[hrow] >= 0) lim[hrow] = min(lim[hrow], qi[hrow] + L - a.Sq);
+        lo[hrow] = (a.window > 0 && qi[hrow] >= 0) ? qi[hrow] + L - a.Sq - a.window + 1 : 0;
+        if (qi[hrow] >= 0) lo_min = min(lo_min, lo[hrow]);
     }
+    // a split wholly below every row's window holds nothing for this tile;
+    // the combine skips it for each row (it reads only splits that reach a
+    // row's window)
+    lo_min = min(lo_min, __shfl_xor_sync(0xffffffffu, lo_min, 4));
+    lo_min = min(lo_min, __shfl_xor_sync(0xffffffffu, lo_min, 8));
+    lo_min = min(lo_min, __shfl_xor_sync(0xffffffffu, lo_min, 16));
+    if (k_hi <= lo_min) return;
 
     const uint32_t wbase = smem_u32(smem) + warp * T::WARP_BYTES;
     const size_t head_off = ((size_t)b * a.Hkv + hkv) * (size_t)a.Sk * D;
-    const uint16_t* kg = a.k + head_off;
-    const uint16_t* vg = a.v + head_off;
+    // element offset of key row `key` of this sequence and key/value head
+    auto row_off = [&](int key) -> size_t {
+        if (!PAGED) return head_off + (size_t)key * D;
+        int page = a.block_table[(size_t)b * a.max_pages + key / a.page_size];
+        page = min(max(page, 0), a.num_pages - 1);
+        return ((size_t)page * a.Hkv + hkv) * (size_t)a.page_size * D +
+               (size_t)(key % a.page_size) * D;
+    };
 
     auto load_block = [&](int i) {
         const int stage = i % T::STAGES;
@@ -127,9 +145,9 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
             const int kr = e / T::GRAN, g = e % T::GRAN;
             const int key = key0 + kr;
             const bool valid = key < k_hi;
-            const size_t src = (size_t)(valid ? key : k_lo) * D + g * 8;
-            cp_async_16(sk + swz<D>(kr, g), kg + src, valid ? 16u : 0u);
-            cp_async_16(sv + swz<D>(kr, g), vg + src, valid ? 16u : 0u);
+            const size_t src = row_off(valid ? key : k_lo) + g * 8;
+            cp_async_16(sk + swz<D>(kr, g), a.k + src, valid ? 16u : 0u);
+            cp_async_16(sv + swz<D>(kr, g), a.v + src, valid ? 16u : 0u);
         }
     };
 
@@ -178,7 +196,7 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
                 for (int e = 0; e < 2; ++e) {
                     const int key = key0 + n * 8 + 2 * (lane & 3) + e;
                     float& sv_ = sacc[n][2 * hrow + e];
-                    sv_ = (key <= lim[hrow]) ? sv_ : -INFINITY;
+                    sv_ = (key <= lim[hrow] && key >= lo[hrow]) ? sv_ : -INFINITY;
                     mx = fmaxf(mx, sv_);
                 }
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -285,7 +303,9 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
     }
 }
 
-// One warp per query row (b, hq, i): LSE-weighted merge of the splits.
+// One warp per query row (b, hq, i): LSE-weighted merge of the splits that
+// reach the row's keys, plus the row's attention sink (one more term of the
+// normaliser without a value) if there is one.
 template <int D>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a) {
     const int lane = threadIdx.x & 31;
@@ -293,19 +313,28 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
     const long long n_rows = (long long)a.B * a.Hq * a.Sq;
     if (row >= n_rows) return;
     const int b = (int)(row / ((long long)a.Hq * a.Sq));
+    const int h = (int)((row / a.Sq) % a.Hq);
+    const int i = (int)(row % a.Sq);
     int L = a.Sk;
     if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[b], a.Sk));
-    const int ns = (L + a.chunk - 1) / a.chunk;   // splits holding keys of this sequence
+    // the row's visible keys [k_first, k_last]
+    int k_last = L - 1;
+    if (a.causal) k_last = min(k_last, i + L - a.Sq);
+    const int k_first = (a.window > 0) ? max(0, i + L - a.Sq - a.window + 1) : 0;
+    const int s_lo = k_first / a.chunk;
+    const int ns = (k_last >= k_first) ? (L + a.chunk - 1) / a.chunk : 0;
     const size_t stride = (size_t)a.B * a.Hq * a.Sq;
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, a.part_lse[s * stride + row]);
+    const float sg = (a.sinks != nullptr) ? a.sinks[h] * kLog2ef : -INFINITY;
+    float M = sg;
+    for (int s = s_lo; s < ns; ++s) M = fmaxf(M, a.part_lse[s * stride + row]);
     constexpr int PER = D / 32;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int s = 0; s < ns; ++s) {
+        wsum = ex2_approx(sg - M);
+        for (int s = s_lo; s < ns; ++s) {
             const float f = ex2_approx(a.part_lse[s * stride + row] - M);
             wsum += f;
             const float* po = a.part_o + (s * stride + row) * D;
@@ -326,11 +355,13 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
 template <int D>
 cudaError_t launch_decode_impl(const DecodeArgs& a, cudaStream_t s) {
     using T = DecodeTraits<D>;
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM);
+    void (*split)(DecodeArgs) =
+        a.block_table != nullptr ? decode_split_kernel<D, true> : decode_split_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(split, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         T::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)a.n_splits, (unsigned)(a.Hkv * a.n_mtiles), (unsigned)a.B);
-    decode_split_kernel<D><<<grid, T::THREADS, T::SMEM, s>>>(a);
+    split<<<grid, T::THREADS, T::SMEM, s>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long rows = (long long)a.B * a.Hq * a.Sq;
@@ -340,12 +371,18 @@ cudaError_t launch_decode_impl(const DecodeArgs& a, cudaStream_t s) {
 
 // ------------------------------------------------------ auxiliary kernels ----
 
-__global__ void fill_empty_kernel(uint16_t* o, float* lse, long long rows, int d) {
+// O = 0 and LSE = -inf (or the row's sink logit: the sink is then the only
+// term of the softmax) for rows without any key.
+__global__ void fill_empty_kernel(uint16_t* o, float* lse, long long rows, int d,
+                                  const float* sinks, int hq, int sq) {
     const long long n = rows * d;
     for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long long)gridDim.x * blockDim.x) {
         o[e] = 0;
-        if (e % d == 0) lse[e / d] = -INFINITY;
+        if (e % d == 0) {
+            const long long row = e / d;
+            lse[row] = (sinks != nullptr) ? sinks[(row / sq) % hq] : -INFINITY;
+        }
     }
 }
 
@@ -376,11 +413,11 @@ cudaError_t launch_decode(const DecodeArgs& a, int head_dim, cudaStream_t s) {
 }
 
 cudaError_t launch_fill_empty(uint16_t* o, float* lse, long long rows, int head_dim,
-                              cudaStream_t s) {
+                              const float* sinks, int hq, int sq, cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     long long blocks = (rows * head_dim + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    fill_empty_kernel<<<(unsigned)blocks, 256, 0, s>>>(o, lse, rows, head_dim);
+    fill_empty_kernel<<<(unsigned)blocks, 256, 0, s>>>(o, lse, rows, head_dim, sinks, hq, sq);
     return cudaGetLastError();
 }
 

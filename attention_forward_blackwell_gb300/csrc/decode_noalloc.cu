@@ -101,7 +101,8 @@ extern "C" fa_status fa_fwd_decode_noalloc(const void* q, const void* k, const v
     if (!slot->supported) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (sk == 0)
-        return launch_fill_empty(static_cast<uint16_t*>(o), lse, (long long)rows, head_dim, s) ==
+        return launch_fill_empty(static_cast<uint16_t*>(o), lse, (long long)rows, head_dim,
+                                 nullptr, hq, sq, s) ==
                        cudaSuccess
                    ? FA_OK
                    : FA_ERR_CUDA;

@@ -59,6 +59,7 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units (a factor of 256)
 constexpr bool kUsePolyExp2 = false;
 constexpr int kPolyEvery = 4;
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
 struct PrefillTraits {
@@ -172,7 +173,7 @@ struct PrefillWork {
     int tail;      // tail unit of the piece (its merge counter)
 };
 
-template <class T, bool CAUSAL>
+template <class T, bool CAUSAL, bool WINDOW>
 __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     PrefillWork w;
     const int c = (int)blockIdx.x;
@@ -203,6 +204,11 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     w.L = L;
     w.off = L - a.Sq;
     w.row0 = mblk * T::NQ * T::BM;
+    if (WINDOW && a.window > 0) {
+        // no row of the unit sees a key below its first row's window
+        const int lo_min = w.row0 + w.off - a.window + 1;
+        if (lo_min > 0) w.kb = max(w.kb, lo_min / T::BN);
+    }
     w.n_kv[0] = w.n_kv[1] = 0;
 #pragma unroll
     for (int t = 0; t < T::NQ; ++t) {
@@ -298,6 +304,13 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         const uint32_t full = smem_u32(&aux->bar_full[slot]);
         const int jk = w.kb + j;          // key block
         const int rv = w.L - jk * T::BN;  // valid rows of this tile
+        // tile coordinates: contiguous K/V, or a page of the paged caches
+        int ty = jk * T::BN, tz = w.b * a.Hkv + w.hk;
+        if (a.block_table != nullptr) {
+            const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
+            ty = ty % a.page_size;
+            tz = page * a.Hkv + w.hk;   // out-of-range pages read as zeros (TMA bounds)
+        }
         if (kv == 1 && j == w.n_max - 1 && rv < T::BN) {
             // Partial last value tile: rows [rv, BN) may hold anything (and a
             // zero probability times a non-finite value would poison O), so
@@ -308,7 +321,7 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 #pragma unroll
                 for (int c = 0; c < T::SLOT_CH; ++c)
                     tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, tm_v,
-                                (pc * T::SLOT_CH + c) * 64, jk * T::BN, w.b * a.Hkv + w.hk, tail);
+                                (pc * T::SLOT_CH + c) * 64, ty, tz, tail);
             }
             if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail)) break;
             zero_value_tail<T>(sRing + slot * T::SLOT, rv);
@@ -319,7 +332,7 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 #pragma unroll
             for (int c = 0; c < T::SLOT_CH; ++c)
                 tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, m, (pc * T::SLOT_CH + c) * 64,
-                            jk * T::BN, w.b * a.Hkv + w.hk, full);
+                            ty, tz, full);
         }
         __syncwarp();
         issued = p + 1;
@@ -543,7 +556,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 
 // ------------------------------------------------------------- softmax ----
 
-template <class T, bool CAUSAL>
+template <class T, bool CAUSAL, bool WINDOW>
 __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillWork& w,
                                      PrefillAux<T>* aux, uint32_t tmem, const WaitCtx& wc,
                                      unsigned long long* tr) {
@@ -556,6 +569,9 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
     int lim = w.L - 1;                                       // last visible key of this row
     if (CAUSAL) lim = min(lim, row + w.off);
     lim -= w.kb * T::BN;   // keys counted from the piece's first key block
+    // first visible key of this row (sliding window), same origin; the
+    // kernels without a window compile none of this
+    const int lo = WINDOW ? row + w.off - a.window + 1 - w.kb * T::BN : 0;
     const float sl2 = a.scale_log2;
     const int nk = w.n_kv[t];
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
@@ -585,12 +601,14 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
         // mask: only tiles that reach past this row's last visible key
         const int kv0 = j * T::BN;   // relative to the piece's first key (lim is too)
-        const bool masked = lim - kv0 < T::BN - 1;
+        const bool masked = lim - kv0 < T::BN - 1 || (WINDOW && lo - kv0 > 0);
         const bool warp_masked = __any_sync(0xffffffffu, masked);
         if (masked) {
-            const int nvis = lim - kv0 + 1;                  // visible columns (may be <= 0)
+            const int nvis = lim - kv0 + 1;                  // visible columns [c0, nvis)
+            const int c0 = WINDOW ? lo - kv0 : 0;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) s[c] = (c < nvis) ? s[c] : -INFINITY;
+            for (int c = 0; c < 128; ++c)
+                s[c] = (c < nvis && (!WINDOW || c >= c0)) ? s[c] : -INFINITY;
         }
         // row max: four independent 3-input-max chains, then combine
         float mq[4];
@@ -724,9 +742,11 @@ __device__ void tail_merge(const PrefillArgs& a, const PrefillWork& w, PrefillAu
         const int row = w.row0 + t * T::BM + r;
         if (row >= a.Sq) continue;
         auto ml_of = [&](int k) { return a.part_ml + ((size_t)(s0 + k) * T::NQ + t) * 2 * T::BM; };
-        float M = -INFINITY;
+        // the sink, if any, joins the merge as one more term without a value
+        const float sg = (a.sinks != nullptr) ? a.sinks[w.h] * kLog2e : -INFINITY;
+        float M = sg;
         for (int k = 0; k < a.split; ++k) M = fmaxf(M, __ldcg(ml_of(k) + r));
-        float L = 0.f;
+        float L = (M == -INFINITY) ? 0.f : ex2_approx(sg - M);
         for (int k = 0; k < a.split; ++k) {
             const float mk = __ldcg(ml_of(k) + r);
             const float wk = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M);
@@ -852,7 +872,21 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             ml[T::BM + r] = (nk > 0) ? l : 0.f;
             continue;
         }
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        // attention sink: one more term e^{sigma} of the normaliser, without a
+        // value; O (accumulated in basis m) is rebased to max(m, sigma)
+        float lf = l, mf = m, oscale = 1.f;
+        if (a.sinks != nullptr) {
+            const float sg = a.sinks[w.h] * kLog2e;
+            const float m2 = fmaxf(m, sg);
+            if (m2 == -INFINITY) {
+                lf = 0.f;
+            } else {
+                oscale = (m == -INFINITY) ? 0.f : ex2_approx(m - m2);
+                lf = l * oscale + ex2_approx(sg - m2);
+                mf = m2;
+            }
+        }
+        const float inv_l = (lf > 0.f) ? oscale / lf : 0.f;
         const uint32_t stage = sQ + t * T::QTILE;
 #pragma unroll 1
         for (int c32 = 0; c32 < (T::D_COLS + 31) / 32; ++c32) {
@@ -882,7 +916,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         }
         const int row = w.row0 + t * T::BM + r;
         if (row < a.Sq) {
-            const float lse = (l > 0.f) ? (m + lg2_approx(l)) * kLn2 : -INFINITY;
+            const float lse = (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
             a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] = lse;
         }
         fence_proxy_async_smem();
@@ -903,7 +937,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
 
 // --------------------------------------------------------------- kernel ----
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool WINDOW>
 __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -918,7 +952,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int wg = warp >> 2;
-    const PrefillWork w = prefill_work<T, CAUSAL>(args);
+    const PrefillWork w = prefill_work<T, CAUSAL, WINDOW>(args);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&aux->bar_q), 1);
@@ -961,7 +995,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
     if (wg < T::NQ) {
         setmaxnreg_inc<T::REG_SOFTMAX>();
-        prefill_softmax_role<T, CAUSAL>(wg, args, w, aux, tmem, wc, tr);
+        prefill_softmax_role<T, CAUSAL, WINDOW>(wg, args, w, aux, tmem, wc, tr);
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::REG_CORR>();
         prefill_correction_role<T>(&tm_o, args, w, aux, tmem, sQ, wc, tr);
@@ -986,7 +1020,8 @@ template <int D>
 cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
     using T = PrefillTraits<D>;
     void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs) =
-        p.causal ? prefill_kernel<D, true> : prefill_kernel<D, false>;
+        p.args.window > 0 ? (p.causal ? prefill_kernel<D, true, true> : prefill_kernel<D, false, true>)
+                          : (p.causal ? prefill_kernel<D, true, false> : prefill_kernel<D, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;

@@ -49,12 +49,12 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("31915540b5bade9598507651c9353eb16e81ca916d98650ad91f05c95a1d8137",
-                118789888, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (463.64 MB) and scaled to batch 64 by the
+    "prefill": ("c947845784b2e6fec8ef6809494a3c5070422c017f541fc6a1cb35f7ab33b83c",
+                119712768, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    # captured at batch 16 (463.75 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
-    "decode": ("ccee9490d466358969a2ce27889455468df8582642f5d88bbe9ebe7b648ca774",
-               2205000000, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    "decode": ("38263356f0cfec74f89a30c674b79a9a3350d63b9f3adcd76105b84ec8be52d0",
+               2205841389, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 

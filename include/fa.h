@@ -91,6 +91,26 @@ fa_status fa_fwd_prefill(const void *q, const void *k, const void *v, void *o,
                          int causal, fa_stream_t stream);
 
 /*
+ * Prefill with a sliding window and/or attention sinks ("2026-05-28_STATUS.md":
+ * D3 "SWA length mask", D4 "causal mask on SWA", D5c "sink merge").
+ *   window  > 0: key j is visible to query row i only if j > i + (L_b - sq) -
+ *           window (with causal: the row's own key and the window - 1 keys
+ *           before it); <= 0: no window.  Query blocks with a window are not
+ *           split across CTAs.
+ *   sinks   NULL, or a device float[hq] (4-byte aligned) of per-query-head
+ *           sink logits in the units of the scaled score: each row's softmax
+ *           becomes e^{s_j} / (e^{sinks[h]} + sum_j e^{s_j}); the sink
+ *           carries no value, and LSE includes it (a row with no visible key
+ *           gets O = 0 and LSE = sinks[h]).
+ * Everything else as fa_fwd_prefill (which is this call with window 0 and
+ * no sinks).
+ */
+fa_status fa_fwd_prefill_ex(const void *q, const void *k, const void *v, void *o,
+                            float *lse, int batch, int hq, int hkv, int sq, int sk,
+                            const int *seqlens_k, int head_dim, float scale, int causal,
+                            int window, const float *sinks, fa_stream_t stream);
+
+/*
  * Decode forward (few queries per sequence against a long key/value cache).
  * Split-KV ("fa4-sm120-research" lists SplitKV among the features its kernels
  * lack; "STAGE_D.md" gives the merge of attention over disjoint key sets by
@@ -108,6 +128,47 @@ fa_status fa_fwd_decode(const void *q, const void *k, const void *v, void *o,
                         float *lse, int batch, int hq, int hkv, int sq, int sk,
                         const int *seqlens_k, int head_dim, float scale,
                         int causal, fa_stream_t stream);
+
+/*
+ * Prefill / decode over paged K/V caches ("fa4-sm120-research" names paged
+ * KV among the features its kernels lack; "2026-05-28_STATUS.md" lists a
+ * paged cache in its KV-cache infrastructure).  The caches are
+ *     k_cache, v_cache : [num_pages, hkv, page_size, head_dim] bf16, 16-byte
+ *                        aligned, caller-owned;
+ *     block_table      : device int32[batch, max_pages]: key j of sequence b
+ *                        is row j % page_size of page
+ *                        block_table[b * max_pages + j / page_size];
+ *     seqlens_k        : device int32[batch], required: L_b keys of sequence
+ *                        b (clamped to [0, max_pages * page_size]).
+ * Only the pages that hold keys j < L_b are read (page indices outside
+ * [0, num_pages) read as zeros in prefill and are clamped in decode).  The
+ * prefill kernel loads 128-key tiles with TMA, so page_size must be a
+ * multiple of 128 (else FA_ERR_UNSUPPORTED); decode takes any page_size >= 1.
+ * Everything else as fa_fwd_prefill / fa_fwd_decode with sk = max_pages *
+ * page_size.  Returns FA_ERR_INVALID_ARG for a NULL block table or seqlens_k,
+ * or non-positive max_pages / page_size / num_pages.
+ */
+fa_status fa_fwd_prefill_paged(const void *q, const void *k_cache, const void *v_cache, void *o,
+                               float *lse, int batch, int hq, int hkv, int sq,
+                               const int *seqlens_k, const int *block_table, int max_pages,
+                               int page_size, int num_pages, int head_dim, float scale,
+                               int causal, fa_stream_t stream);
+fa_status fa_fwd_decode_paged(const void *q, const void *k_cache, const void *v_cache, void *o,
+                              float *lse, int batch, int hq, int hkv, int sq,
+                              const int *seqlens_k, const int *block_table, int max_pages,
+                              int page_size, int num_pages, int head_dim, float scale,
+                              int causal, fa_stream_t stream);
+
+/*
+ * Decode with a sliding window and/or attention sinks: the same window and
+ * sink semantics as fa_fwd_prefill_ex (for sq = 1 the window keeps the last
+ * `window` keys of each sequence).  Splits wholly below a row's window are
+ * not read.  Everything else as fa_fwd_decode.
+ */
+fa_status fa_fwd_decode_ex(const void *q, const void *k, const void *v, void *o,
+                           float *lse, int batch, int hq, int hkv, int sq, int sk,
+                           const int *seqlens_k, int head_dim, float scale, int causal,
+                           int window, const float *sinks, fa_stream_t stream);
 
 /*
  * fa_fwd_decode with an explicit number of key splits (num_splits <= 0 picks
