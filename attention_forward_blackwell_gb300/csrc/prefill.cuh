@@ -157,7 +157,8 @@ __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int
 //
 // The grid is one-dimensional.  Its first n_full CTAs each process a whole
 // unit (batch entry, query head, query block), in the order query block
-// (fastest; heaviest first when causal), head, batch entry.  The remaining
+// (fastest), head, batch entry; causal units in the order (batch entry, head)
+// fastest, then query block heaviest first.  The remaining
 // units (the last, partial wave of a grid of whole units) are each split
 // along the key axis into `split` pieces of consecutive key blocks, one CTA
 // per piece, so that the last wave is `split` times shorter; the pieces write
@@ -193,8 +194,13 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
         ke = (int)((long long)(k + 1) * a.nk / a.split);
         w.piece = q;
     }
-    const int x = u % a.num_mblk;
-    const int hb = u / a.num_mblk;
+    // Causal: query block slowest, heaviest first over every (batch, head), so
+    // that the hardware's in-order dispatch to free SMs is a longest-first
+    // schedule.  Non-causal units are equal: query block fastest, so that the
+    // CTAs running at once share the K/V of few heads in L2.
+    const int nbh = a.B * a.Hq;
+    const int x = CAUSAL ? u / nbh : u % a.num_mblk;
+    const int hb = CAUSAL ? u % nbh : u / a.num_mblk;
     const int mblk = CAUSAL ? (a.num_mblk - 1 - x) : x;
     w.h = hb % a.Hq;
     w.b = hb / a.Hq;
