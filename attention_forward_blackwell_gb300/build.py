@@ -23,6 +23,12 @@ FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", CSRC, "-I", INCLUDE]
 
 
+def _options():
+    """Build options from the environment: FA_PREFILL_TRACE=1 compiles the
+    prefill kernel's debug clock trace (off by default: it costs registers)."""
+    return ["-DFA_PREFILL_TRACE=1"] if os.environ.get("FA_PREFILL_TRACE") == "1" else []
+
+
 def _nvcc():
     for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
         if cand and (os.path.sep not in cand or os.path.exists(cand)):
@@ -40,7 +46,7 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
     os.makedirs(OBJDIR, exist_ok=True)
     # objects from another host architecture (or toolchain) are never reused
     stamp = os.path.join(OBJDIR, "host.txt")
-    host = f"{platform.machine()} {platform.system()}"
+    host = f"{platform.machine()} {platform.system()} {' '.join(_options())}"
     if not os.path.exists(stamp) or open(stamp).read() != host:
         force = True
     nvcc = _nvcc()
@@ -52,7 +58,7 @@ def build(force: bool = False, jobs: int | None = None, verbose: bool = False) -
         if (not force and os.path.exists(o)
                 and os.path.getmtime(o) >= max(os.path.getmtime(s), newest_header)):
             return o, False
-        cmd = [nvcc] + FLAGS + ["-c", s, "-o", o + ".tmp"]
+        cmd = [nvcc] + FLAGS + _options() + ["-c", s, "-o", o + ".tmp"]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)

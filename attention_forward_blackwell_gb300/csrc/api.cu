@@ -452,6 +452,7 @@ fa_status fa_selftest_exp2_poly(const float* x, float* y, int n, fa_stream_t str
 
 fa_status fa_debug_prefill_trace(unsigned long long* buf, int block) {
     if (buf != nullptr && block < 0) return FA_ERR_INVALID_ARG;
+    if (buf != nullptr && !FA_PREFILL_TRACE) return FA_ERR_UNSUPPORTED;
     g_trace_buf = buf;
     g_trace_block = block;
     return FA_OK;

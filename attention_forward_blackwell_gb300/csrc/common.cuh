@@ -58,6 +58,9 @@ struct PrefillArgs {
     int trace_block;
 };
 
+#ifndef FA_PREFILL_TRACE
+#define FA_PREFILL_TRACE 0   // 1: compile the prefill kernel's clock trace
+#endif
 // Trace layout: kTraceSlots stamps per role; role r, event e of iteration j
 // lands at trace[r * kTraceSlots + j * kTraceEvents + e].
 constexpr int kTraceSlots = 4096;

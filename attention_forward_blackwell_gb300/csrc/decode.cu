@@ -397,7 +397,7 @@ __global__ void wait_timeout_selftest_kernel(unsigned int* err_word, unsigned lo
         mbar_fence_init();
     }
     __syncthreads();
-    const WaitCtx wc{&abort_flag, err_word, limit_ns};
+    const WaitCtx wc{smem_u32(&abort_flag), (uint32_t)limit_ns, err_word};
     mbar_wait(smem_u32(&bar), 0, wc, kErrWaitTimeout | 0xFFu);
 }
 

@@ -127,7 +127,6 @@ struct PrefillAux {
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
     uint64_t bar_split_a;          // piece of a split unit: partial result written (4 warps)
-    uint64_t bar_split_b;          // arrival counted; merge decision posted
     uint32_t tmem_base;
     int abort_flag;
     int merge_last;
@@ -140,7 +139,7 @@ struct PrefillAux {
 enum : unsigned int {
     kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
-    kSiteEpiStage, kSiteSplitA, kSiteSplitB
+    kSiteEpiStage, kSiteSplitA
 };
 
 // Recorded if a piece's arrival could not be counted (never expected: every
@@ -148,8 +147,10 @@ enum : unsigned int {
 constexpr unsigned int kErrSplitCount = 0x2001u;
 
 // Debug trace stamp (SM clock) by the calling thread, if tracing this CTA.
+// Compiled in only with FA_PREFILL_TRACE=1 (otherwise the trace pointer is
+// dead code and occupies no registers).
 __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int j, int e) {
-    if (tr != nullptr && j * kTraceEvents + e < kTraceSlots)
+    if (FA_PREFILL_TRACE && tr != nullptr && j * kTraceEvents + e < kTraceSlots)
         tr[role * kTraceSlots + j * kTraceEvents + e] = (unsigned long long)clock64();
 }
 
@@ -162,7 +163,7 @@ __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int
 // units (the last, partial wave of a grid of whole units) are each split
 // along the key axis into `split` pieces of consecutive key blocks, one CTA
 // per piece, so that the last wave is `split` times shorter; the pieces write
-// partial results and the last one to finish merges them (tail_merge).
+// partial results and the last one to finish merges them (merge_unit).
 // Key-block counters below are local to the CTA's piece: block j of the
 // piece is key block kb + j.
 struct PrefillWork {
@@ -360,33 +361,35 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
 // Descriptor address offset (bytes >> 4) of K-step kk inside a K-major
 // operand stored as 64-column chunks of 128 rows: chunk kk/4, then 32 bytes
 // per step inside the 128-byte swizzled row.
-__device__ __forceinline__ constexpr uint64_t kstep_off(int kk) {
-    return (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4);
+__device__ __forceinline__ constexpr uint32_t kstep_off(int kk) {
+    return (uint32_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4);
 }
 
 // Score MMA S[128 x 128] = Q_t K_j^T: one N = 128 instruction per K-step of
 // 16 head dims.  qd: descriptor of the Q tile; kd[p]: descriptors of the ring
-// slots that hold the K tile (two slots for head_dim 256).
+// slots that hold the K tile (two slots for head_dim 256).  Descriptors are
+// passed as their lower 32-bit words (sdesc_lo_sw128): one add per operand
+// per instruction on the issuing thread, and half the registers.
 template <class T>
-__device__ __forceinline__ void issue_score(uint32_t tmem_d, uint64_t qd,
-                                            const uint64_t (&kd)[T::PIECES], uint32_t idesc) {
+__device__ __forceinline__ void issue_score(uint32_t tmem_d, uint32_t qd,
+                                            const uint32_t (&kd)[T::PIECES], uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < T::KSTEPS; ++kk) {
         const int piece = kk / (T::SLOT_CH * 4);
         const int kin = kk % (T::SLOT_CH * 4);
-        umma_ss(tmem_d, qd + kstep_off(kk), kd[piece] + kstep_off(kin), idesc, kk > 0 ? 1u : 0u);
+        umma_ss_lo(tmem_d, qd + kstep_off(kk), kd[piece] + kstep_off(kin), idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 // Value MMA O[:, 0:N] (+)= P V over 128 keys: 8 steps of 16 keys.  V is
 // MN-major: 16 keys are two 8-row swizzle atoms, 2048 bytes per step.
 template <class T>
-__device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, uint64_t vd,
+__device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, uint32_t vd,
                                             uint32_t idesc, bool first) {
 #pragma unroll
     for (int kk = 0; kk < T::BN / 16; ++kk)
-        umma_ts(tmem_o, tmem_p + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), idesc,
-                (!first || kk > 0) ? 1u : 0u);
+        umma_ts_lo(tmem_o, tmem_p + kk * 8, vd + (uint32_t)((kk * 2048) >> 4), idesc,
+                   (!first || kk > 0) ? 1u : 0u);
 }
 
 // MMA issue: one elected lane of one warp issues every tcgen05.mma of the CTA
@@ -421,18 +424,18 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     };
     // descriptors of the Q tiles and of ring slot 0, built once; everything
     // else is an address offset added to them
-    const uint64_t qd0 = sdesc_sw128(sQ, 16, 1024);            // K-major Q
-    const uint64_t kd0 = sdesc_sw128(sRing, 16, 1024);         // K-major K
-    const uint64_t vd0 = sdesc_sw128(sRing, T::CHUNK, 1024);   // MN-major V
-    auto qdesc = [&](int t) { return qd0 + (uint64_t)((t * T::QTILE) >> 4); };
-    auto slot_off = [&](int p) { return (uint64_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
-    auto kdesc = [&](int p0, uint64_t (&kd)[T::PIECES]) {
+    const uint32_t qd0 = sdesc_lo_sw128(sQ, 16);             // K-major Q
+    const uint32_t kd0 = sdesc_lo_sw128(sRing, 16);          // K-major K
+    const uint32_t vd0 = sdesc_lo_sw128(sRing, T::CHUNK);    // MN-major V
+    auto qdesc = [&](int t) { return qd0 + (uint32_t)((t * T::QTILE) >> 4); };
+    auto slot_off = [&](int p) { return (uint32_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
+    auto kdesc = [&](int p0, uint32_t (&kd)[T::PIECES]) {
 #pragma unroll
         for (int pc = 0; pc < T::PIECES; ++pc) kd[pc] = kd0 + slot_off(p0 + pc);
     };
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
-    uint64_t kd[T::PIECES];
+    uint32_t kd[T::PIECES];
 
     if (w.n_max > 0) do {
         if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
@@ -705,84 +708,102 @@ __device__ __forceinline__ void store_o32(uint16_t* orow, const float (&v)[32], 
     }
 }
 
-// Arrival of a piece of a split unit (after its partial result is in
-// scratch) and, for the last piece to arrive, the merge: the pieces' O, row
-// max and row sum are rebased to their common max and added (the same
-// recurrence as between key blocks), then O / row_sum and LSE are stored.
-// No CTA waits for another: the counter tells each piece whether it is last.
+// Arrival of a piece of a split unit, once its partial result (unnormalised
+// O, row max, row sum) is in scratch: the pieces count themselves on the
+// unit's counter, and the one that arrives last sets aux->merge_last; its CTA
+// then merges the unit at the end of the kernel (merge_unit, all threads).
+// No CTA waits for another.
 template <class T>
-__device__ void tail_merge(const PrefillArgs& a, const PrefillWork& w, PrefillAux<T>* aux, int r,
-                           const WaitCtx& wc) {
+__device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, PrefillAux<T>* aux,
+                             const WaitCtx& wc) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     mbar_arrive_warp(smem_u32(&aux->bar_split_a));   // this warp's stores issued
-    bool ok = true;
-    if (warp == T::CORR_WG * 4) {
-        ok = mbar_wait(smem_u32(&aux->bar_split_a), 0, wc, kErrWaitTimeout | kSiteSplitA);
-        if (ok && lane == 0) {
-            __threadfence();   // this piece's stores (all four warps) before the count
-            unsigned long long* cp = a.part_count + w.tail;
-            const unsigned long long tag = a.epoch << 16;
-            unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cp);
-            unsigned long long arrived = 0;
-            for (int attempt = 0; attempt <= a.split; ++attempt) {
-                const unsigned long long cur = ((old >> 16) == a.epoch) ? (old & 0xffffull) : 0ull;
-                const unsigned long long prev = atomicCAS(cp, old, tag | (cur + 1));
-                if (prev == old) {
-                    arrived = cur + 1;
-                    break;
-                }
-                old = prev;
-            }
-            if (arrived == 0) record_error(wc, kErrSplitCount);
-            __threadfence();   // the other pieces' stores before this piece's loads
-            *reinterpret_cast<volatile int*>(&aux->merge_last) =
-                arrived == (unsigned long long)a.split ? 1 : 0;
-            mbar_arrive(smem_u32(&aux->bar_split_b));
+    if (warp != T::CORR_WG * 4) return;
+    if (!mbar_wait(smem_u32(&aux->bar_split_a), 0, wc, kErrWaitTimeout | kSiteSplitA) || lane != 0)
+        return;
+    __threadfence();   // this piece's stores (all four warps) before the count
+    unsigned long long* cp = a.part_count + w.tail;
+    const unsigned long long tag = a.epoch << 16;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cp);
+    unsigned long long arrived = 0;
+    for (int attempt = 0; attempt <= a.split; ++attempt) {
+        const unsigned long long cur = ((old >> 16) == a.epoch) ? (old & 0xffffull) : 0ull;
+        const unsigned long long prev = atomicCAS(cp, old, tag | (cur + 1));
+        if (prev == old) {
+            arrived = cur + 1;
+            break;
         }
+        old = prev;
     }
-    if (!ok || !mbar_wait(smem_u32(&aux->bar_split_b), 0, wc, kErrWaitTimeout | kSiteSplitB)) return;
-    if (!*reinterpret_cast<volatile int*>(&aux->merge_last)) return;
+    if (arrived == 0) record_error(wc, kErrSplitCount);
+    __threadfence();   // the other pieces' stores before this CTA's loads
+    aux->merge_last = arrived == (unsigned long long)a.split ? 1 : 0;
+}
+
+// Merge of split unit w.tail once all its pieces' partial results are in
+// scratch: each piece's O, row max and row sum are rebased to the running
+// max and added (the streaming recurrence again, over pieces instead of key
+// blocks; the sink, if any, is one more term without a value), then
+// O / row_sum and LSE are stored.  The work (rows x 16-column groups, rows
+// fastest so that loads coalesce) is dealt to threads tid = 0 .. nthr-1; a
+// thread's loads for one piece do not depend on the previous piece, so two
+// pieces' loads are in flight at once.
+template <class T>
+__device__ void merge_unit(const PrefillArgs& a, const PrefillWork& w, int tid, int nthr) {
+    constexpr int NC16 = T::D_COLS / 16;
     const int s0 = w.tail * a.split;
+    const float sg = (a.sinks != nullptr) ? a.sinks[w.h] * kLog2e : -INFINITY;
 #pragma unroll 1
-    for (int t = 0; t < T::NQ; ++t) {
+    for (int task = tid; task < T::NQ * NC16 * T::BM; task += nthr) {
+        const int r = task % T::BM;
+        const int c16 = (task / T::BM) % NC16;
+        const int t = task / (T::BM * NC16);
         const int row = w.row0 + t * T::BM + r;
         if (row >= a.Sq) continue;
-        auto ml_of = [&](int k) { return a.part_ml + ((size_t)(s0 + k) * T::NQ + t) * 2 * T::BM; };
-        // the sink, if any, joins the merge as one more term without a value
-        const float sg = (a.sinks != nullptr) ? a.sinks[w.h] * kLog2e : -INFINITY;
         float M = sg;
-        for (int k = 0; k < a.split; ++k) M = fmaxf(M, __ldcg(ml_of(k) + r));
-        float L = (M == -INFINITY) ? 0.f : ex2_approx(sg - M);
+        float L = (sg == -INFINITY) ? 0.f : 1.f;
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll 2
         for (int k = 0; k < a.split; ++k) {
-            const float mk = __ldcg(ml_of(k) + r);
-            const float wk = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M);
-            L = fmaf(wk, __ldcg(ml_of(k) + T::BM + r), L);
+            const size_t slot = (size_t)(s0 + k) * T::NQ + t;
+            const float* ml = a.part_ml + slot * 2 * T::BM;
+            const float4* po = reinterpret_cast<const float4*>(a.part_o + slot * (T::D_COLS * T::BM));
+            const float mk = __ldcg(ml + r);
+            const float lk = __ldcg(ml + T::BM + r);
+            float4 x[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) x[q] = __ldcg(po + (size_t)(c16 * 4 + q) * T::BM + r);
+            if (mk == -INFINITY) continue;   // a piece without keys adds nothing
+            const float m2 = fmaxf(M, mk);
+            const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - m2);
+            const float wk = ex2_approx(mk - m2);
+            M = m2;
+            L = fmaf(L, sc, wk * lk);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[4 * q + 0] = fmaf(acc[4 * q + 0], sc, wk * x[q].x);
+                acc[4 * q + 1] = fmaf(acc[4 * q + 1], sc, wk * x[q].y);
+                acc[4 * q + 2] = fmaf(acc[4 * q + 2], sc, wk * x[q].z);
+                acc[4 * q + 3] = fmaf(acc[4 * q + 3], sc, wk * x[q].w);
+            }
         }
         const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
-        uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * T::D_COLS;
-#pragma unroll 1
-        for (int c32 = 0; c32 < T::D_COLS / 32; ++c32) {
-            float acc[32];
+        uint4* dst = reinterpret_cast<uint4*>(
+            a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * T::D_COLS + c16 * 16);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            for (int k = 0; k < a.split; ++k) {
-                const float mk = __ldcg(ml_of(k) + r);
-                const float wk = (mk == -INFINITY) ? 0.f : ex2_approx(mk - M);
-                const float4* po = reinterpret_cast<const float4*>(
-                    a.part_o + ((size_t)(s0 + k) * T::NQ + t) * (T::D_COLS * T::BM));
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 x = __ldcg(po + (size_t)(c32 * 8 + q) * T::BM + r);
-                    acc[4 * q + 0] = fmaf(wk, x.x, acc[4 * q + 0]);
-                    acc[4 * q + 1] = fmaf(wk, x.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(wk, x.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(wk, x.w, acc[4 * q + 3]);
-                }
-            }
-            store_o32(orow + c32 * 32, acc, inv_l);
+        for (int h = 0; h < 2; ++h) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[8 * h + 0] * inv_l, acc[8 * h + 1] * inv_l);
+            v.y = pack_bf16x2(acc[8 * h + 2] * inv_l, acc[8 * h + 3] * inv_l);
+            v.z = pack_bf16x2(acc[8 * h + 4] * inv_l, acc[8 * h + 5] * inv_l);
+            v.w = pack_bf16x2(acc[8 * h + 6] * inv_l, acc[8 * h + 7] * inv_l);
+            dst[h] = v;
         }
-        a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
-            (L > 0.f) ? (M + lg2_approx(L)) * kLn2 : -INFINITY;
+        if (c16 == 0)
+            a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+                (L > 0.f) ? (M + lg2_approx(L)) * kLn2 : -INFINITY;
     }
 }
 
@@ -938,7 +959,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
     }
     if (issuer) bulk_wait_group_0();
-    if (ok && w.piece >= 0) tail_merge<T>(a, w, aux, r, wc);
+    if (ok && w.piece >= 0) split_arrive<T>(a, w, aux, wc);
 }
 
 // --------------------------------------------------------------- kernel ----
@@ -981,7 +1002,6 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         mbar_init(smem_u32(&aux->bar_drain[1]), 1);
         mbar_init(smem_u32(&aux->bar_tail), 1);
         mbar_init(smem_u32(&aux->bar_split_a), 4);
-        mbar_init(smem_u32(&aux->bar_split_b), 1);
         aux->abort_flag = 0;
         aux->merge_last = 0;
         mbar_fence_init();
@@ -994,9 +1014,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = aux->tmem_base;
-    const WaitCtx wc{&aux->abort_flag, args.err_word, args.wait_limit_ns};
+    const WaitCtx wc{smem_u32(&aux->abort_flag), (uint32_t)args.wait_limit_ns, args.err_word};
     const int block_lin = blockIdx.x;
-    unsigned long long* tr = (args.trace != nullptr && block_lin == args.trace_block) ? args.trace
+    unsigned long long* tr =
+        (FA_PREFILL_TRACE && args.trace != nullptr && block_lin == args.trace_block) ? args.trace
                                                                                      : nullptr;
 
     if (wg < T::NQ) {
@@ -1019,6 +1040,9 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, T::TMEM_COLS);
     }
+    // the last piece of a split unit to arrive merges it, on all threads
+    if (w.piece >= 0 && aux->merge_last != 0 && ld_volatile_shared(wc.abort_flag) == 0)
+        merge_unit<T>(args, w, (int)threadIdx.x, T::THREADS);
 }
 
 // Host-side launch of one head-dimension instantiation.

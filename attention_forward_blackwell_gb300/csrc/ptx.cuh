@@ -21,6 +21,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Low 32 bits of the global nanosecond timer (differences are exact up to
+// 4.29 s, modulo 2^32).
+__device__ __forceinline__ uint32_t globaltimer_lo() {
+    uint32_t t;
+    asm volatile("mov.u32 %0, %%globaltimer_lo;" : "=r"(t));
+    return t;
+}
+__device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
+    int v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_volatile_shared(uint32_t addr, int v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -75,17 +90,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Shared state of the bounded waits of one CTA: a time limit, a CTA-wide
 // abort flag in shared memory and the device error word in global memory.
+// Kept small (four registers) because every wait site is inlined.
 struct WaitCtx {
-    volatile int* abort_flag;   // shared memory; nonzero once any role gave up
+    uint32_t abort_flag;        // shared-memory address of an int; nonzero once any role gave up
+    uint32_t limit_ns;          // time limit of one wait (below 2^32 ns)
     unsigned int* err_word;     // global memory; first error code wins
-    uint64_t limit_ns;
 };
 
 // Records an error code once per device word and raises the CTA abort flag.
 // The word holds the code in bits 0-15 and the (linear) CTA index in bits
 // 16-31, so a time-out names the CTA whose wait gave up first.
 __device__ __forceinline__ void record_error(const WaitCtx& w, unsigned int code) {
-    *w.abort_flag = 1;
+    st_volatile_shared(w.abort_flag, 1);
     const unsigned int cta = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
     atomicCAS(w.err_word, 0u, (code & 0xFFFFu) | ((cta & 0xFFFFu) << 16));
 }
@@ -96,12 +112,12 @@ __device__ __forceinline__ void record_error(const WaitCtx& w, unsigned int code
 __device__ __forceinline__ bool mbar_wait_lane(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                unsigned int code) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint32_t t0 = globaltimer_lo();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0u) {
-            if (*w.abort_flag) return false;
-            if (globaltimer_ns() - t0 > w.limit_ns) {
+            if (ld_volatile_shared(w.abort_flag)) return false;
+            if (globaltimer_lo() - t0 > w.limit_ns) {
                 record_error(w, code);
                 return false;
             }
@@ -225,14 +241,51 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 // offset (32-45, >>4), descriptor version 1 (bit 46), swizzle mode 2 =
 // 128-byte (bits 61-63).  Swizzle atoms must start on 1024-byte boundaries;
 // the start address may be advanced inside an atom along K.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes,
-                                                uint32_t sbo_bytes) {
+__host__ __device__ constexpr uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo_bytes,
+                                                   uint32_t sbo_bytes) {
     uint64_t d = (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// The same descriptor split in two 32-bit words.  Every operand here has a
+// 1024-byte stride offset, so the upper word is one constant; the lower word
+// (start address and leading byte offset) is advanced with 32-bit adds (a
+// start address below 256 KB never carries into bit 14).
+constexpr uint32_t kSdescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);
+__host__ __device__ constexpr uint32_t sdesc_lo_sw128(uint32_t smem_addr, uint32_t lbo_bytes) {
+    return ((smem_addr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+static_assert(((uint64_t)kSdescHiSw128 << 32 | sdesc_lo_sw128(0x3FC00u, 16)) ==
+                  sdesc_sw128(0x3FC00u, 16, 1024),
+              "split descriptor differs from the 64-bit one");
+static_assert(((uint64_t)kSdescHiSw128 << 32 | sdesc_lo_sw128(0x12400u, 128 * 128)) ==
+                  sdesc_sw128(0x12400u, 128 * 128, 1024),
+              "split descriptor differs from the 64-bit one");
+// umma_ss / umma_ts with descriptors given by their lower words.
+__device__ __forceinline__ void umma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 da, {%1, %5};\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHiSw128)
+        : "memory");
+}
+__device__ __forceinline__ void umma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kSdescHiSw128)
+        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp reads lane

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(128) mma_tile_kernel(const uint16_t* a, const 
         tc_commit(smem_u32(&bar));
     }
     __syncwarp();
-    const WaitCtx wc{&abort_flag, err_word, 1000000000ull};
+    const WaitCtx wc{smem_u32(&abort_flag), 1000000000u, err_word};
     const bool ok = mbar_wait(smem_u32(&bar), 0, wc, kErrWaitTimeout | 0xFEu);
     tc_fence_after();
     if (ok) {

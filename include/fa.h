@@ -280,8 +280,11 @@ fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t str
  * CTA with linear index `block` (x + gridDim.x * (y + gridDim.y * z)) record
  * SM clock stamps at its pipeline events: role r (0 MMA issue, 1 and 2
  * softmax of query tile 0 and 1, 3 correction/epilogue, 4 TMA producer),
- * event e of key/value iteration j at buf[r * 4096 + j * 16 + e].  Unused
- * slots are left untouched.  buf = NULL switches tracing off.
+ * event e of key/value iteration j at buf[r * 4096 + j * 16 + e], for the
+ * CTA's first work item.  Unused slots are left untouched.  buf = NULL
+ * switches tracing off.  The stamps are compiled in only when the library is
+ * built with FA_PREFILL_TRACE=1 (the Python build reads it from the
+ * environment); otherwise a non-NULL buf returns FA_ERR_UNSUPPORTED.
  */
 fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
 
