@@ -88,15 +88,22 @@ struct PrefillTraits {
     // Register split (threads x registers after setmaxnreg must not exceed
     // the launch allocation: 512 x 128 for NQ = 2, 384 x 168 for NQ = 1).
     // Every target differs from the launch count (increase or decrease).
-    static constexpr uint32_t REG_SOFTMAX = (NQ == 2) ? 168 : 240;
-    static constexpr uint32_t REG_CORR = (NQ == 2) ? 88 : 88;
-    static constexpr uint32_t REG_OTHER = (NQ == 2) ? 88 : 80;
+    // NQ = 2 has two splits, chosen per kernel by measurement on GB300: the
+    // kernels with masked scores (causal or windowed) run fastest with 176
+    // registers per softmax thread (no spills; the MMA-issue and TMA warps
+    // need under 72), the unmasked one with 168 / 88 / 88.
     static constexpr uint32_t LAUNCH_REGS = (NQ == 2) ? 128 : 168;
-    static_assert(REG_SOFTMAX > LAUNCH_REGS && REG_CORR < LAUNCH_REGS && REG_OTHER < LAUNCH_REGS,
-                  "setmaxnreg targets must move away from the launch allocation");
-    static_assert(4 * NQ * 32 * REG_SOFTMAX + 4 * 32 * REG_CORR + 4 * 32 * REG_OTHER <=
-                      THREADS * LAUNCH_REGS,
-                  "register split exceeds the launch allocation");
+    template <bool MASKED>
+    struct Regs {
+        static constexpr uint32_t SOFTMAX = (NQ == 2) ? (MASKED ? 176 : 168) : 240;
+        static constexpr uint32_t CORR = 88;
+        static constexpr uint32_t OTHER = (NQ == 2) ? (MASKED ? 72 : 88) : 80;
+        static_assert(SOFTMAX > LAUNCH_REGS && CORR < LAUNCH_REGS && OTHER < LAUNCH_REGS,
+                      "setmaxnreg targets must move away from the launch allocation");
+        static_assert(4 * NQ * 32 * SOFTMAX + 4 * 32 * CORR + 4 * 32 * OTHER <=
+                          (NQ + 2) * 128 * LAUNCH_REGS,
+                      "register split exceeds the launch allocation");
+    };
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
@@ -130,6 +137,7 @@ struct PrefillAux {
     uint32_t tmem_base;
     int abort_flag;
     int merge_last;
+    int merge_unit[4];             // tail, head, batch entry, first row of the unit to merge
     float mb_alpha[2][128];
     float mb_l[T::NQ][128];
     float mb_m[T::NQ][128];
@@ -737,6 +745,12 @@ __device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, Prefill
     }
     if (arrived == 0) record_error(wc, kErrSplitCount);
     __threadfence();   // the other pieces' stores before this CTA's loads
+    // what the merge needs, kept in shared memory rather than live in
+    // registers through every role
+    aux->merge_unit[0] = w.tail;
+    aux->merge_unit[1] = w.h;
+    aux->merge_unit[2] = w.b;
+    aux->merge_unit[3] = w.row0;
     aux->merge_last = arrived == (unsigned long long)a.split ? 1 : 0;
 }
 
@@ -748,17 +762,19 @@ __device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, Prefill
 // fastest so that loads coalesce) is dealt to threads tid = 0 .. nthr-1; a
 // thread's loads for one piece do not depend on the previous piece, so two
 // pieces' loads are in flight at once.
+// Unit: split index `tail`, query head h, batch entry b, first row row0.
 template <class T>
-__device__ void merge_unit(const PrefillArgs& a, const PrefillWork& w, int tid, int nthr) {
+__device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row0, int tid,
+                           int nthr) {
     constexpr int NC16 = T::D_COLS / 16;
-    const int s0 = w.tail * a.split;
-    const float sg = (a.sinks != nullptr) ? a.sinks[w.h] * kLog2e : -INFINITY;
+    const int s0 = tail * a.split;
+    const float sg = (a.sinks != nullptr) ? a.sinks[h] * kLog2e : -INFINITY;
 #pragma unroll 1
     for (int task = tid; task < T::NQ * NC16 * T::BM; task += nthr) {
         const int r = task % T::BM;
         const int c16 = (task / T::BM) % NC16;
         const int t = task / (T::BM * NC16);
-        const int row = w.row0 + t * T::BM + r;
+        const int row = row0 + t * T::BM + r;
         if (row >= a.Sq) continue;
         float M = sg;
         float L = (sg == -INFINITY) ? 0.f : 1.f;
@@ -791,7 +807,7 @@ __device__ void merge_unit(const PrefillArgs& a, const PrefillWork& w, int tid, 
         }
         const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(
-            a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * T::D_COLS + c16 * 16);
+            a.o + (((size_t)b * a.Hq + h) * a.Sq + row) * T::D_COLS + c16 * 16);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint4 v;
@@ -802,12 +818,15 @@ __device__ void merge_unit(const PrefillArgs& a, const PrefillWork& w, int tid, 
             dst[h] = v;
         }
         if (c16 == 0)
-            a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+            a.lse[((size_t)b * a.Hq + h) * a.Sq + row] =
                 (L > 0.f) ? (M + lg2_approx(L)) * kLn2 : -INFINITY;
     }
 }
 
-template <class T>
+// SPLIT: the instantiation can receive pieces of split units (only the
+// unmasked, unwindowed one: the work split never cuts causal or windowed
+// units, whose lengths differ); the others compile none of that code.
+template <class T, bool SPLIT>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
                                         const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
                                         uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
@@ -873,7 +892,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             }
             tc_fence_after();
         }
-        if (w.piece >= 0) {
+        if (SPLIT && w.piece >= 0) {
             // a piece of a split unit: unnormalised O, row max and row sum
             // -> this piece's scratch slot (merged below)
             float4* po = reinterpret_cast<float4*>(
@@ -959,7 +978,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
     }
     if (issuer) bulk_wait_group_0();
-    if (ok && w.piece >= 0) split_arrive<T>(a, w, aux, wc);
+    if (SPLIT && ok && w.piece >= 0) split_arrive<T>(a, w, aux, wc);
 }
 
 // --------------------------------------------------------------- kernel ----
@@ -1021,13 +1040,13 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
                                                                                      : nullptr;
 
     if (wg < T::NQ) {
-        setmaxnreg_inc<T::REG_SOFTMAX>();
+        setmaxnreg_inc<T::template Regs<CAUSAL || WINDOW>::SOFTMAX>();
         prefill_softmax_role<T, CAUSAL, WINDOW>(wg, args, w, aux, tmem, wc, tr);
     } else if (wg == T::CORR_WG) {
-        setmaxnreg_dec<T::REG_CORR>();
-        prefill_correction_role<T>(&tm_o, args, w, aux, tmem, sQ, wc, tr);
+        setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
+        prefill_correction_role<T, !CAUSAL && !WINDOW>(&tm_o, args, w, aux, tmem, sQ, wc, tr);
     } else {
-        setmaxnreg_dec<T::REG_OTHER>();
+        setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
         if (warp == T::MMA_WARP)
             prefill_mma_role<T>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
         else if (warp == T::LOAD_WARP)
@@ -1041,8 +1060,9 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         tmem_dealloc(tmem, T::TMEM_COLS);
     }
     // the last piece of a split unit to arrive merges it, on all threads
-    if (w.piece >= 0 && aux->merge_last != 0 && ld_volatile_shared(wc.abort_flag) == 0)
-        merge_unit<T>(args, w, (int)threadIdx.x, T::THREADS);
+    if (!CAUSAL && !WINDOW && aux->merge_last != 0 && ld_volatile_shared(wc.abort_flag) == 0)
+        merge_unit<T>(args, aux->merge_unit[0], aux->merge_unit[1], aux->merge_unit[2],
+                      aux->merge_unit[3], (int)threadIdx.x, T::THREADS);
 }
 
 // Host-side launch of one head-dimension instantiation.

@@ -49,12 +49,12 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("c947845784b2e6fec8ef6809494a3c5070422c017f541fc6a1cb35f7ab33b83c",
-                119712768, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (463.75 MB) and scaled to batch 64 by the
+    "prefill": ("7920eba7c754e431afe6d8e4844046457dfcebe40c16ea35bab242b7843e407c",
+                118872832, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    # captured at batch 16 (464.04 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
-    "decode": ("38263356f0cfec74f89a30c674b79a9a3350d63b9f3adcd76105b84ec8be52d0",
-               2205841389, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    "decode": ("5c1327045f6450ecac2e1a3c45158b8537f264704503be54a57ade84124eb8cc",
+               2207221023, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 
