@@ -32,6 +32,8 @@ SIGNATURES = {
                                   _I, _F, _I, _VP]),
     "fa_fwd_decode_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _I, _I,
                                  _I, _F, _I, _VP]),
+    "fa_fwd_prefill_varlen": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
+                                   _I, _F, _I, _I, _VP, _VP]),
     "fa_fwd_decode": (_I, _FWD + [_VP]),
     "fa_fwd_decode_splits": (_I, _FWD + [_I, _VP]),
     "fa_fwd_decode_noalloc": (_I, _FWD + [_VP]),
@@ -125,10 +127,10 @@ def _outputs(q, out, lse):
     return out, lse
 
 
-def _check_sinks(sinks, q):
+def _check_sinks(sinks, hq):
     if sinks is None:
         return None
-    if sinks.dtype != torch.float32 or sinks.shape != (q.shape[1],) or not sinks.is_cuda:
+    if sinks.dtype != torch.float32 or sinks.shape != (hq,) or not sinks.is_cuda:
         raise ValueError("sinks must be a CUDA fp32 tensor of shape [Hq]")
     return sinks.contiguous()
 
@@ -140,7 +142,7 @@ def prefill(q, k, v, scale=None, causal=False, seqlens_k=None, out=None, lse=Non
     B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
     out, lse = _outputs(q, out, lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    sinks = _check_sinks(sinks, q)
+    sinks = _check_sinks(sinks, q.shape[1])
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk,
             _ptr(seqlens_k), d, scale, int(bool(causal)))
     if (window and window > 0) or sinks is not None:
@@ -160,7 +162,7 @@ def decode(q, k, v, scale=None, causal=False, seqlens_k=None, num_splits=0, out=
     B, Hq, Hkv, Sq, Sk, d, seqlens_k = _check_inputs(q, k, v, seqlens_k)
     out, lse = _outputs(q, out, lse)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    sinks = _check_sinks(sinks, q)
+    sinks = _check_sinks(sinks, q.shape[1])
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk,
             _ptr(seqlens_k), d, scale, int(bool(causal)))
     if (window and window > 0) or sinks is not None:
@@ -201,6 +203,47 @@ def _paged(name, q, k_cache, v_cache, block_table, seqlens_k, scale, causal, out
                               _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, name)
+    return out, lse
+
+
+def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale=None,
+                   causal=False, window=0, sinks=None, out=None, lse=None, stream=None):
+    """Prefill over packed sequences through ``fa_fwd_prefill_varlen``:
+    q [total_q, Hq, d], k and v [total_k, Hkv, d] bf16, int32 offsets
+    cu_seqlens_q / cu_seqlens_k [B + 1]; returns o [total_q, Hq, d] and
+    lse [Hq, total_q]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or t.dim() != 3:
+            raise ValueError(f"{n} must be a CUDA bf16 tensor [tokens, heads, d]")
+    total_q, Hq, d = q.shape
+    total_k, Hkv, dk = k.shape
+    if v.shape != k.shape or dk != d:
+        raise ValueError("k and v must be [total_k, Hkv, d] with q's d")
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        if not t.is_cuda or t.dtype != torch.int32 or t.dim() != 1:
+            raise ValueError(f"{n} must be a CUDA int32 vector [B + 1]")
+    if cu_seqlens_q.shape != cu_seqlens_k.shape or cu_seqlens_q.numel() < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be [B + 1]")
+    B = cu_seqlens_q.numel() - 1
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    cu_seqlens_q, cu_seqlens_k = cu_seqlens_q.contiguous(), cu_seqlens_k.contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, total_q, device=q.device, dtype=torch.float32)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (Hq, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [Hq, total_q]")
+    sinks = _check_sinks(sinks, Hq)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().fa_fwd_prefill_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                     _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, int(max_seqlen_q),
+                                     int(max_seqlen_k), total_q, total_k, Hq, Hkv, d, scale,
+                                     int(bool(causal)), int(window), _ptr(sinks),
+                                     _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_prefill_varlen")
     return out, lse
 
 

@@ -91,15 +91,24 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // 3-D bf16 tensor map over [planes][rows][d] with a {64, 128, 1} box and
 // 128-byte swizzle (rows past `rows` and columns past `d` read as zero).
-bool encode_map(CUtensorMap* m, const void* base, int d, int rows, long long planes) {
+// 3-D bf16 map {d, rows, planes} with a 64 x 128 x 1 box and 128-byte swizzle.
+// Strides in bytes: row_stride between rows, plane_stride between planes
+// (contiguous [planes][rows][d] when they are d * 2 and rows * d * 2).
+bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
+                        unsigned long long row_stride, unsigned long long plane_stride) {
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
-    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)rows * d * 2};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)plane_stride};
     const cuuint32_t box[3] = {64, 128, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_map(CUtensorMap* m, const void* base, int d, int rows, long long planes) {
+    return encode_map_strided(m, base, d, rows, planes, (unsigned long long)d * 2,
+                              (unsigned long long)rows * d * 2);
 }
 
 struct Common {
@@ -216,11 +225,20 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
 
 // Prefill on contiguous K/V (block_table == nullptr) or on paged caches
 // [num_pages, hkv, page_size, d] (sk = max_pages * page_size keys per sequence).
+// Packed variable-length sequences (see fa_fwd_prefill_varlen).
+struct Varlen {
+    const int* cu_seqlens_q;
+    const int* cu_seqlens_k;
+    int total_q, total_k;
+};
+
+// Dense, paged (block_table != nullptr) or packed (vl != nullptr; sq is then
+// the largest query length and sk the largest key length) prefill.
 fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
                        int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
                        float scale, int causal, int window, const float* sinks,
                        const int* block_table, int max_pages, int page_size, int num_pages,
-                       fa_stream_t stream) {
+                       fa_stream_t stream, const Varlen* vl = nullptr) {
     Common c;
     fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
     if (st != FA_OK || c.noop) return st;
@@ -231,19 +249,40 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     if (!di) return FA_ERR_CUDA;
     if (!di->supported) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (sk == 0)
-        return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
-                                           (long long)batch * hq * sq, head_dim, sinks, hq, sq,
-                                           s));
-    PrefillLaunch p;
-    const int kv_rows = block_table ? page_size : sk;
-    const long long kv_planes = block_table ? (long long)num_pages * hkv : (long long)batch * hkv;
-    if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
-        !encode_map(&p.tm_k, k, head_dim, kv_rows, kv_planes) ||
-        !encode_map(&p.tm_v, v, head_dim, kv_rows, kv_planes) ||
-        !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
-        return FA_ERR_INVALID_ARG;
+    if (sk == 0 || (vl && vl->total_k == 0)) {
+        // no keys anywhere: O = 0 and LSE = -inf (or the sink); for packed
+        // sequences, O [total_q, hq, d] and LSE [hq, total_q] read as one
+        // sequence of total_q rows
+        const long long rows = vl ? (long long)vl->total_q * hq : (long long)batch * hq * sq;
+        return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse, rows, head_dim, sinks,
+                                           hq, vl ? vl->total_q : sq, s));
+    }
+    PrefillLaunch p{};
+    const unsigned long long row_bytes = (unsigned long long)head_dim * 2;
+    if (vl) {
+        // token-major packed tensors: map {d, tokens, heads}, a token's heads adjacent
+        if (!encode_map_strided(&p.tm_q, q, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes) ||
+            !encode_map_strided(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
+            !encode_map_strided(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
+            !encode_map_strided(&p.tm_o, o, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes))
+            return FA_ERR_INVALID_ARG;
+    } else {
+        const int kv_rows = block_table ? page_size : sk;
+        const long long kv_planes =
+            block_table ? (long long)num_pages * hkv : (long long)batch * hkv;
+        if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
+            !encode_map(&p.tm_k, k, head_dim, kv_rows, kv_planes) ||
+            !encode_map(&p.tm_v, v, head_dim, kv_rows, kv_planes) ||
+            !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
+            return FA_ERR_INVALID_ARG;
+    }
     PrefillArgs& a = p.args;
+    if (vl) {
+        a.cu_seqlens_q = vl->cu_seqlens_q;
+        a.cu_seqlens_k = vl->cu_seqlens_k;
+        a.total_q = vl->total_q;
+        a.total_k = vl->total_k;
+    }
     a.o = static_cast<uint16_t*>(o);
     a.lse = lse;
     a.seqlens_k = seqlens_k;
@@ -272,7 +311,9 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
     a.nk = (sk + 127) / 128;
     // (a windowed unit has fewer key blocks than nk: it is not split either)
-    const PrefillPlan plan = plan_prefill(units, a.nk, p.causal || a.window > 0, di->num_sms);
+    // (packed sequences have units of different lengths: not split either)
+    const PrefillPlan plan =
+        plan_prefill(units, a.nk, p.causal || a.window > 0 || vl != nullptr, di->num_sms);
     a.n_full = plan.n_full;
     a.split = plan.split;
     p.n_tail = plan.n_tail;
@@ -335,6 +376,28 @@ fa_status fa_fwd_prefill_paged(const void* q, const void* k_cache, const void* v
     return prefill_impl(q, k_cache, v_cache, o, lse, batch, hq, hkv, sq, max_pages * page_size,
                         seqlens_k, head_dim, scale, causal, 0, nullptr, block_table, max_pages,
                         page_size, num_pages, stream);
+}
+
+fa_status fa_fwd_prefill_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                                const int* cu_seqlens_q, const int* cu_seqlens_k, int batch,
+                                int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                                int hq, int hkv, int head_dim, float scale, int causal,
+                                int window, const float* sinks, fa_stream_t stream) {
+    if (batch < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0)
+        return FA_ERR_INVALID_ARG;
+    if (batch == 0 || total_q == 0 || hq == 0) return FA_OK;   // nothing to compute
+    if (max_seqlen_q == 0 || (total_k > 0 && max_seqlen_k == 0)) return FA_ERR_INVALID_ARG;
+    if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(cu_seqlens_k) & 3u) != 0)
+        return FA_ERR_MISALIGNED;
+    if ((long long)total_q * hq * head_dim >= (1ll << 40) ||
+        (long long)total_k * hkv * head_dim >= (1ll << 40))
+        return FA_ERR_INVALID_ARG;
+    const Varlen vl{cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+    return prefill_impl(q, k, v, o, lse, batch, hq, hkv, max_seqlen_q,
+                        total_k > 0 ? max_seqlen_k : 0, nullptr, head_dim, scale, causal, window,
+                        sinks, nullptr, 0, 0, 0, stream, &vl);
 }
 
 fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -35,6 +35,14 @@ struct PrefillArgs {
     const int* block_table;
     int max_pages;
     int page_size;
+    // Packed variable-length sequences (nullptr: dense): sequence b owns
+    // query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) of Q, O [total_q, Hq, d]
+    // and keys [cu_seqlens_k[b], cu_seqlens_k[b+1]) of K, V [total_k, Hkv, d];
+    // LSE is [Hq, total_q].  Offsets are clamped to [0, total] in the kernel.
+    // Sq is then the largest query length (units per (b, h) = num_mblk).
+    const int* cu_seqlens_q;
+    const int* cu_seqlens_k;
+    int total_q, total_k;
     int num_mblk;               // query blocks (units) per (b, h)
     // Work split (see prefill_work): CTAs [0, n_full) process whole units;
     // each later unit is split into `split` pieces of its nk key blocks.

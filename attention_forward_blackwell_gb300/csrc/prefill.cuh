@@ -181,9 +181,12 @@ struct PrefillWork {
     int kb;        // first key block of the piece (0 for a whole unit)
     int piece;     // -1 for a whole unit, else the piece's scratch slot
     int tail;      // tail unit of the piece (its merge counter)
+    // packed sequences only: query rows of the sequence, and its first query
+    // token and first key token in the packed tensors
+    int Lq, q0, k0;
 };
 
-template <class T, bool CAUSAL, bool WINDOW>
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
 __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     PrefillWork w;
     const int c = (int)blockIdx.x;
@@ -215,9 +218,24 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
     w.b = hb / a.Hq;
     w.hk = w.h / a.group;
     int L = a.Sk;
-    if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[w.b], a.Sk));
+    if constexpr (VARLEN) {
+        // sequence b's tokens, clamped so that malformed offsets stay inside
+        // the packed tensors
+        const int qs = min(max(a.cu_seqlens_q[w.b], 0), a.total_q);
+        const int qe = min(max(a.cu_seqlens_q[w.b + 1], qs), a.total_q);
+        const int ks = min(max(a.cu_seqlens_k[w.b], 0), a.total_k);
+        const int ke = min(max(a.cu_seqlens_k[w.b + 1], ks), a.total_k);
+        w.q0 = qs;
+        w.k0 = ks;
+        w.Lq = qe - qs;
+        L = ke - ks;
+        w.off = L - w.Lq;
+    } else {
+        // (Lq, q0, k0 are read by the packed-sequence kernels only)
+        if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[w.b], a.Sk));
+        w.off = L - a.Sq;
+    }
     w.L = L;
-    w.off = L - a.Sq;
     w.row0 = mblk * T::NQ * T::BM;
     if (WINDOW && a.window > 0) {
         // no row of the unit sees a key below its first row's window
@@ -232,6 +250,8 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
         const int n = last >= 0 ? last / T::BN + 1 : 0;
         const int cnt = min(n, ke) - w.kb;
         w.n_kv[t] = cnt > 0 ? cnt : 0;
+        // a tile past the end of its sequence has nothing to compute
+        if (VARLEN && w.row0 + t * T::BM >= w.Lq) w.n_kv[t] = 0;
     }
     w.n_max = max(w.n_kv[0], w.n_kv[T::NQ - 1]);
     return w;
@@ -284,7 +304,7 @@ __device__ __forceinline__ void zero_value_tail(uint32_t slot_addr, int rv) {
 
 // ------------------------------------------------------------ producer ----
 
-template <class T>
+template <class T, bool VARLEN>
 __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, const PrefillArgs& a,
                                   const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
@@ -302,8 +322,9 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         for (int t = 0; t < T::NQ; ++t)
 #pragma unroll
             for (int c = 0; c < T::NCH; ++c)
-                tma_load_3d(sQ + t * T::QTILE + c * T::CHUNK, tm_q, c * 64, w.row0 + t * T::BM,
-                            w.b * a.Hq + w.h, bar_q);
+                tma_load_3d(sQ + t * T::QTILE + c * T::CHUNK, tm_q, c * 64,
+                            (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
+                            VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
     }
     int issued = 0;
     const int total = 2 * w.n_max * T::PIECES;
@@ -320,7 +341,8 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         const int jk = w.kb + j;          // key block
         const int rv = w.L - jk * T::BN;  // valid rows of this tile
         // tile coordinates: contiguous K/V, or a page of the paged caches
-        int ty = jk * T::BN, tz = w.b * a.Hkv + w.hk;
+        // (packed sequences: token k0 + j of head hk)
+        int ty = (VARLEN ? w.k0 : 0) + jk * T::BN, tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
         if (a.block_table != nullptr) {
             const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
             ty = ty % a.page_size;
@@ -403,7 +425,7 @@ __device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, ui
 // MMA issue: one elected lane of one warp issues every tcgen05.mma of the CTA
 // and the commits that release K/V slots and signal the softmax/correction
 // warpgroups.
-template <class T>
+template <class T, bool VARLEN>
 __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork& w,
                                  PrefillAux<T>* aux, uint32_t tmem, uint32_t sQ, uint32_t sRing,
                                  const WaitCtx& wc, unsigned long long* tr) {
@@ -486,7 +508,10 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                                        vd0 + slot_off(posV), idesc_v, j == 0);
                         tc_commit(smem_u32(&aux->bar_pv_done[t]));
                     }
-                    if (t == 1) release_tile(posV, false);   // V_j fully consumed
+                    // V_j fully consumed after the last tile that uses it (tile 1,
+                    // or tile 0 alone when tile 1 has no block j: a packed
+                    // sequence may end inside tile 0)
+                    if (t == 1 || (VARLEN && j >= w.n_kv[1])) release_tile(posV, false);
                     trace_mark(tr, kTrMma, j, 2 + 3 * t);
                     if (j + 1 < w.n_kv[t]) {
                         if (!k_next_ready) {
@@ -826,7 +851,7 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
 // SPLIT: the instantiation can receive pieces of split units (only the
 // unmasked, unwindowed one: the work split never cuts causal or windowed
 // units, whose lengths differ); the others compile none of that code.
-template <class T, bool SPLIT>
+template <class T, bool SPLIT, bool VARLEN>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
                                         const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
                                         uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
@@ -934,6 +959,12 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         }
         const float inv_l = (lf > 0.f) ? oscale / lf : 0.f;
         const uint32_t stage = sQ + t * T::QTILE;
+        const int row = w.row0 + t * T::BM + r;
+        // packed sequences: a tile that runs past the end of its sequence is
+        // stored row by row (a TMA store would write the next sequence's rows)
+        const bool direct = VARLEN && w.row0 + t * T::BM + T::BM > w.Lq;
+        uint16_t* orow =
+            VARLEN ? a.o + ((size_t)(w.q0 + row) * a.Hq + w.h) * T::D_COLS : nullptr;
 #pragma unroll 1
         for (int c32 = 0; c32 < (T::D_COLS + 31) / 32; ++c32) {
             uint32_t v[32];
@@ -954,25 +985,34 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 for (int e = 0; e < 4; ++e)
                     pk[e] = pack_bf16x2(__uint_as_float(v[g4 * 8 + 2 * e]) * inv_l,
                                         __uint_as_float(v[g4 * 8 + 2 * e + 1]) * inv_l);
+                if (VARLEN && direct) {
+                    if (row < w.Lq)
+                        *reinterpret_cast<uint4*>(orow + c32 * 32 + g4 * 8) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    continue;
+                }
                 const uint32_t addr = row_addr + ((uint32_t)(g ^ (r & 7)) << 4);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[0]),
                              "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                              : "memory");
             }
         }
-        const int row = w.row0 + t * T::BM + r;
-        if (row < a.Sq) {
+        if (row < (VARLEN ? w.Lq : a.Sq)) {
             const float lse = (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
-            a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] = lse;
+            if constexpr (VARLEN)
+                a.lse[(size_t)w.h * a.total_q + w.q0 + row] = lse;   // [Hq, total_q]
+            else
+                a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] = lse;
         }
         fence_proxy_async_smem();
         mbar_arrive_warp(smem_u32(&aux->bar_epi[t]));
-        if (issuer && w.row0 + t * T::BM < a.Sq &&
+        if (issuer && !direct && w.row0 + t * T::BM < (VARLEN ? w.Lq : a.Sq) &&
             mbar_wait_lane(smem_u32(&aux->bar_epi[t]), 0, wc, kErrWaitTimeout | kSiteEpiStage)) {
 #pragma unroll
             for (int ch = 0; ch < T::NCH; ++ch)
-                tma_store_3d(tm_o, stage + ch * T::CHUNK, ch * 64, w.row0 + t * T::BM,
-                             w.b * a.Hq + w.h);
+                tma_store_3d(tm_o, stage + ch * T::CHUNK, ch * 64,
+                             (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
+                             VARLEN ? w.h : w.b * a.Hq + w.h);
             bulk_commit_group();
         }
         trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
@@ -983,7 +1023,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
 
 // --------------------------------------------------------------- kernel ----
 
-template <int D, bool CAUSAL, bool WINDOW>
+template <int D, bool CAUSAL, bool WINDOW, bool VARLEN>
 __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -998,7 +1038,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int wg = warp >> 2;
-    const PrefillWork w = prefill_work<T, CAUSAL, WINDOW>(args);
+    const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, VARLEN>(args);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&aux->bar_q), 1);
@@ -1044,13 +1084,14 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         prefill_softmax_role<T, CAUSAL, WINDOW>(wg, args, w, aux, tmem, wc, tr);
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
-        prefill_correction_role<T, !CAUSAL && !WINDOW>(&tm_o, args, w, aux, tmem, sQ, wc, tr);
+        prefill_correction_role<T, !CAUSAL && !WINDOW && !VARLEN, VARLEN>(&tm_o, args, w, aux, tmem,
+                                                                          sQ, wc, tr);
     } else {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
         if (warp == T::MMA_WARP)
-            prefill_mma_role<T>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
+            prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
         else if (warp == T::LOAD_WARP)
-            prefill_load_role<T>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc, tr);
+            prefill_load_role<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc, tr);
     }
 
     tc_fence_before();
@@ -1060,18 +1101,29 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         tmem_dealloc(tmem, T::TMEM_COLS);
     }
     // the last piece of a split unit to arrive merges it, on all threads
-    if (!CAUSAL && !WINDOW && aux->merge_last != 0 && ld_volatile_shared(wc.abort_flag) == 0)
+    if (!CAUSAL && !WINDOW && !VARLEN && aux->merge_last != 0 &&
+        ld_volatile_shared(wc.abort_flag) == 0)
         merge_unit<T>(args, aux->merge_unit[0], aux->merge_unit[1], aux->merge_unit[2],
                       aux->merge_unit[3], (int)threadIdx.x, T::THREADS);
 }
 
 // Host-side launch of one head-dimension instantiation.
+using PrefillKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs);
+
+template <int D, bool VARLEN>
+PrefillKernelFn pick_prefill_kernel(bool causal, bool window) {
+    return window ? (causal ? prefill_kernel<D, true, true, VARLEN> : prefill_kernel<D, false, true, VARLEN>)
+                  : (causal ? prefill_kernel<D, true, false, VARLEN>
+                            : prefill_kernel<D, false, false, VARLEN>);
+}
+
 template <int D>
 cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
     using T = PrefillTraits<D>;
-    void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs) =
-        p.args.window > 0 ? (p.causal ? prefill_kernel<D, true, true> : prefill_kernel<D, false, true>)
-                          : (p.causal ? prefill_kernel<D, true, false> : prefill_kernel<D, false, false>);
+    const bool window = p.args.window > 0;
+    const PrefillKernelFn kern = p.args.cu_seqlens_q != nullptr
+                                     ? pick_prefill_kernel<D, true>(p.causal, window)
+                                     : pick_prefill_kernel<D, false>(p.causal, window);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;

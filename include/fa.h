@@ -160,6 +160,36 @@ fa_status fa_fwd_decode_paged(const void *q, const void *k_cache, const void *v_
                               int causal, fa_stream_t stream);
 
 /*
+ * Prefill over packed variable-length sequences ("b200-flash-attention4-
+ * planner", section B, lists variable-length packed sequences among the
+ * extensions its forward design leaves open).  Sequence b owns query tokens
+ * [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key tokens
+ * [cu_seqlens_k[b], cu_seqlens_k[b+1]); each sequence is attended on its own,
+ * exactly as fa_fwd_prefill_ex with batch 1, sq = its query length and
+ * sk = its key length (causal alignment bottom-right, the same window and
+ * sink semantics).  Layouts (bf16, 16-byte aligned, caller-owned):
+ *     q, o         : [total_q, hq, head_dim]   (token-major, heads adjacent)
+ *     k, v         : [total_k, hkv, head_dim]
+ *     lse          : [hq, total_q] fp32
+ *     cu_seqlens_q : device int32[batch + 1], nondecreasing, [0] = 0,
+ *                    [batch] = total_q; cu_seqlens_k likewise with total_k.
+ * max_seqlen_q / max_seqlen_k must be at least every sequence's query / key
+ * length (the launch covers max_seqlen_q query rows per sequence; rows of a
+ * longer sequence beyond that are not written).  Offsets are clamped to
+ * [0, total] on the device, so malformed offsets never address memory outside
+ * the tensors.  Sequences without keys give O = 0 and LSE = -inf (or the
+ * sink).  head_dim 64, 96, 128 or 256.  Returns FA_ERR_INVALID_ARG for
+ * negative sizes, NULL offsets, or max_seqlen_q = 0 with total_q > 0;
+ * FA_ERR_MISALIGNED for offsets not 4-byte aligned.
+ */
+fa_status fa_fwd_prefill_varlen(const void *q, const void *k, const void *v, void *o,
+                                float *lse, const int *cu_seqlens_q, const int *cu_seqlens_k,
+                                int batch, int max_seqlen_q, int max_seqlen_k, int total_q,
+                                int total_k, int hq, int hkv, int head_dim, float scale,
+                                int causal, int window, const float *sinks,
+                                fa_stream_t stream);
+
+/*
  * Decode with a sliding window and/or attention sinks: the same window and
  * sink semantics as fa_fwd_prefill_ex (for sq = 1 the window keeps the last
  * `window` keys of each sequence).  Splits wholly below a row's window are
