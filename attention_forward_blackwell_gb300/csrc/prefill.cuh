@@ -187,9 +187,8 @@ struct PrefillWork {
 };
 
 template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
-__device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a) {
+__device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a, int c) {
     PrefillWork w;
-    const int c = (int)blockIdx.x;
     int u, ke;
     if (c < a.n_full) {
         u = c;
@@ -304,7 +303,7 @@ __device__ __forceinline__ void zero_value_tail(uint32_t slot_addr, int rv) {
 
 // ------------------------------------------------------------ producer ----
 
-template <class T, bool VARLEN>
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
 __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                   const CUtensorMap* tm_v, const PrefillArgs& a,
                                   const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
@@ -1017,7 +1016,8 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         }
         trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
     }
-    if (issuer) bulk_wait_group_0();
+    // the CTA may exit once the O stores have read shared memory
+    if (issuer) bulk_wait_group_read_0();
     if (SPLIT && ok && w.piece >= 0) split_arrive<T>(a, w, aux, wc);
 }
 
@@ -1038,7 +1038,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int wg = warp >> 2;
-    const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, VARLEN>(args);
+    const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, VARLEN>(args, (int)blockIdx.x);
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&aux->bar_q), 1);
@@ -1091,7 +1091,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         if (warp == T::MMA_WARP)
             prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
         else if (warp == T::LOAD_WARP)
-            prefill_load_role<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc, tr);
+            prefill_load_role<T, CAUSAL, WINDOW, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ,
+                                                         sRing, wc, tr);
     }
 
     tc_fence_before();

@@ -149,6 +149,13 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
+// Waits until every committed bulk store of this thread has read its
+// shared-memory source (the global writes may still be in flight; they are
+// visible to later work once the kernel has completed).
+__device__ __forceinline__ void bulk_wait_group_read_0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // 3-D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int x, int y,
                                             int z, uint32_t bar) {
