@@ -76,6 +76,38 @@ def test_decode_specific_validation(lib):
                              None) == 2
 
 
+P_MIS4 = ctypes.c_void_p((1 << 12) + 2)   # not 4-byte aligned
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (q, k, v, o, lse, cu_q, cu_k, B, max_q, max_k, total_q, total_k, Hq, Hkv, d, scale,
+    #  causal, window, sinks), status
+    ((P16, P16, P16, P16, P16, P16, P16, -1, 8, 8, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 1),
+    ((P16, P16, P16, P16, P16, P16, P16, 2, 0, 8, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 1),
+    ((P16, P16, P16, P16, P16, P16, P16, 2, 8, 0, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 1),
+    ((P16, P16, P16, P16, P16, None, P16, 2, 8, 8, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 1),
+    ((P16, P16, P16, P16, P16, P_MIS4, P16, 2, 8, 8, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 3),
+    ((P16, P16, P16, P16, P16, P16, P16, 2, 8, 8, 8, 8, 3, 2, 64, 1.0, 0, 0, None), 1),
+    ((P16, P16, P16, P16, P16, P16, P16, 2, 8, 8, 8, 8, 2, 1, 80, 1.0, 0, 0, None), 2),
+    ((P_ODD, P16, P16, P16, P16, P16, P16, 2, 8, 8, 8, 8, 2, 1, 64, 1.0, 0, 0, None), 3),
+    ((None, None, None, None, None, None, None, 0, 0, 0, 0, 0, 2, 1, 64, 1.0, 0, 0, None), 0),
+    ((None, None, None, None, None, None, None, 3, 0, 0, 0, 0, 2, 1, 64, 1.0, 0, 0, None), 0),
+])
+def test_varlen_host_validation(lib, args, expect):
+    """Packed-sequence argument checks run on the host, before any launch."""
+    assert lib.fa_fwd_prefill_varlen(*args, None) == expect
+
+
+def test_paged_host_validation(lib):
+    # (q, kc, vc, o, lse, B, Hq, Hkv, Sq, seqlens, table, max_pages, page, pages, d, scale, causal)
+    ok = (P16, P16, P16, P16, P16, 1, 2, 1, 4, P16, P16, 2, 128, 4, 64, 1.0, 0)
+    bad_table = ok[:10] + (None,) + ok[11:]
+    bad_page = ok[:12] + (100,) + ok[13:]
+    assert lib.fa_fwd_prefill_paged(*bad_table, None) == 1           # no block table
+    assert lib.fa_fwd_prefill_paged(*bad_page, None) == 2            # tile must fit a page
+    assert lib.fa_fwd_decode_paged(*(ok[:13] + (0,) + ok[14:]), None) == 1   # no pages
+
+
 def test_binding_rejects_bad_tensors():
     import torch
     from attention_forward_blackwell_gb300 import binding
