@@ -768,6 +768,11 @@ __device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, Prefill
         old = prev;
     }
     if (arrived == 0) record_error(wc, kErrSplitCount);
+    // The last piece resets the counter (no other piece touches it again in
+    // this launch), so that a replay of a captured launch -- same scratch
+    // address, same epoch -- starts from zero.
+    if (arrived == (unsigned long long)a.split)
+        *reinterpret_cast<volatile unsigned long long*>(cp) = 0ull;
     __threadfence();   // the other pieces' stores before this CTA's loads
     // what the merge needs, kept in shared memory rather than live in
     // registers through every role

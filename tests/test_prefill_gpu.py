@@ -238,3 +238,31 @@ def test_split_units_are_deterministic():
     for _ in range(5):
         o2, l2 = _run(x, 0.088, False)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_units_replay_in_a_cuda_graph():
+    """A launch with split units (last-arriver merge, per-launch counters)
+    captured in a CUDA graph and replayed: every replay equals the eager
+    result bit for bit (the last piece resets its counter)."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(1, 2, 2, 4096, 4096, 128, tag=990, device="cuda")
+    assert binding.debug_prefill_plan(1, 2, 4096, 4096, 128, 0, 152)[2] > 1   # split
+    o_ref, l_ref = binding.prefill(x.q, x.k, x.v)
+    o = torch.empty_like(x.q)
+    lse = torch.empty(1, 2, 4096, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up outside the capture
+        binding.prefill(x.q, x.k, x.v, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.prefill(x.q, x.k, x.v, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        check_device_error()
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
