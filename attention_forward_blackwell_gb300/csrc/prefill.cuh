@@ -34,8 +34,14 @@
 // different accumulators are not ordered by the ISA, so the MMA warp issues
 // S_t(j+1) only once PV_t(j) has completed (tcgen05.commit -> mbarrier); the
 // tensor core is busy with that PV while the warp waits.  Descriptors are
-// built once per CTA and advanced by address offsets, so each MMA issue is a
-// few integer adds and the instruction itself.
+// built once per CTA as their lower 32-bit words and advanced by address
+// offsets, so each MMA issue is one add per operand and the instruction
+// itself (the issuing thread's instruction count sets the pace).
+//
+// Work split: one CTA per unit; when the units do not fill the last wave,
+// those of the last partial wave are cut along the key axis into pieces that
+// write unnormalised partial results, and the last piece to arrive merges
+// them on all threads of its CTA after its roles finish (merge_unit).
 //
 // Rebasing: the running max m is only moved when the block max exceeds it by
 // more than kRescaleThreshold (log2 units).  Until then P = exp2(s - m) may
