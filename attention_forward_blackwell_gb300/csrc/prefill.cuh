@@ -95,15 +95,15 @@ struct PrefillTraits {
     // the launch allocation: 512 x 128 for NQ = 2, 384 x 168 for NQ = 1).
     // Every target differs from the launch count (increase or decrease).
     // NQ = 2 has two splits, chosen per kernel by measurement on GB300: the
-    // kernels with masked scores (causal or windowed) run fastest with 176
-    // registers per softmax thread (no spills; the MMA-issue and TMA warps
-    // need under 72), the unmasked one with 168 / 88 / 88.
+    // kernels with masked scores (causal or windowed) run fastest with
+    // 176 / 88 / 72 (no spills; the MMA-issue and TMA warps need under 72),
+    // the unmasked one with 168 / 96 / 80.
     static constexpr uint32_t LAUNCH_REGS = (NQ == 2) ? 128 : 168;
     template <bool MASKED>
     struct Regs {
         static constexpr uint32_t SOFTMAX = (NQ == 2) ? (MASKED ? 176 : 168) : 240;
-        static constexpr uint32_t CORR = 88;
-        static constexpr uint32_t OTHER = (NQ == 2) ? (MASKED ? 72 : 88) : 80;
+        static constexpr uint32_t CORR = (NQ == 2 && !MASKED) ? 96 : 88;
+        static constexpr uint32_t OTHER = (NQ == 2) ? (MASKED ? 72 : 80) : 80;
         static_assert(SOFTMAX > LAUNCH_REGS && CORR < LAUNCH_REGS && OTHER < LAUNCH_REGS,
                       "setmaxnreg targets must move away from the launch allocation");
         static_assert(4 * NQ * 32 * SOFTMAX + 4 * 32 * CORR + 4 * 32 * OTHER <=
