@@ -49,12 +49,12 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("7920eba7c754e431afe6d8e4844046457dfcebe40c16ea35bab242b7843e407c",
-                118872832, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (464.04 MB) and scaled to batch 64 by the
+    "prefill": ("e67ed15139b168cca1d6f28d33f98e41b00346ee1a7e8f5af7913cf42f021a24",
+                118334976, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    # captured at batch 16 (464.13 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
-    "decode": ("5c1327045f6450ecac2e1a3c45158b8537f264704503be54a57ade84124eb8cc",
-               2207221023, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    "decode": ("c3984c96d483e09007206d223eb17d584e4da8584d32db373e192416e68b34e6",
+               2207660607, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 
