@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -195,21 +196,26 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     a.num_pages = num_pages;
     a.scale_log2 = scale * 1.4426950408889634f;
     if ((long long)hkv * a.n_mtiles > 65535) return FA_ERR_INVALID_ARG;
-    // split planning: equal chunks of a multiple of 64 keys
+    // split planning: equal chunks of a multiple of 64 keys over the keys a
+    // sequence's rows can see: all sk, or with a sliding window the last
+    // window + sq - 1 (the splits start at each sequence's first visible key,
+    // rounded down to a multiple of 64: up to 63 more)
+    const long long span = a.window > 0 ? std::min<long long>(sk, (long long)a.window + sq + 62)
+                                        : (long long)sk;
     int splits = num_splits;
     if (splits <= 0) {
         const long long pairs = (long long)batch * hkv * a.n_mtiles;
         const long long target = 24ll * di->num_sms;   // CTAs worth keeping in flight
         long long want = (target + pairs - 1) / pairs;
-        const long long max_splits = (sk + 255) / 256;  // at least 256 keys per split
+        const long long max_splits = (span + 255) / 256;  // at least 256 keys per split
         if (want > max_splits) want = max_splits;
         if (want < 1) want = 1;
         splits = (int)want;
     }
-    long long chunk = ((long long)sk + splits - 1) / splits;
+    long long chunk = (span + splits - 1) / splits;
     chunk = (chunk + 63) / 64 * 64;
     a.chunk = (int)chunk;
-    a.n_splits = (int)((sk + chunk - 1) / chunk);
+    a.n_splits = (int)((span + chunk - 1) / chunk);
     const size_t rows = (size_t)batch * hq * sq;
     const size_t bytes_o = (size_t)a.n_splits * rows * head_dim * sizeof(float);
     const size_t bytes_l = (size_t)a.n_splits * rows * sizeof(float);

@@ -67,7 +67,11 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
     const int b = blockIdx.z;
     int L = a.Sk;
     if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[b], a.Sk));
-    const int k_lo = split * a.chunk;
+    // splits start at the first key any query row of the sequence can see,
+    // rounded down to a multiple of 64 (with a sliding window, the keys
+    // before it are never read; the rounding keeps 16-key slices aligned)
+    const int k_base = (a.window > 0) ? (max(0, L - a.Sq - a.window + 1) & ~63) : 0;
+    const int k_lo = k_base + split * a.chunk;
     if (k_lo >= L) return;                       // nothing of this sequence here
     const int k_hi = min(k_lo + a.chunk, L);
     const int nblk = (k_hi - k_lo + T::KB - 1) / T::KB;
@@ -135,17 +139,23 @@ __global__ void __launch_bounds__(DecodeTraits<D>::THREADS)
                (size_t)(key % a.page_size) * D;
     };
 
+    // paged caches whose pages hold whole 16-key slices (slices start at
+    // multiples of 16): one page lookup per slice instead of one per row
+    const bool slice_pages = PAGED && a.page_size % T::KB == 0;
+
     auto load_block = [&](int i) {
         const int stage = i % T::STAGES;
         const int key0 = k_lo + T::KB * (warp + T::WARPS * i);
         const uint32_t sk = wbase + stage * 2 * T::SLICE;
         const uint32_t sv = sk + T::SLICE;
+        const size_t slice_off = slice_pages ? row_off(key0) : 0;
 #pragma unroll
         for (int e = lane; e < T::KB * T::GRAN; e += 32) {
             const int kr = e / T::GRAN, g = e % T::GRAN;
             const int key = key0 + kr;
             const bool valid = key < k_hi;
-            const size_t src = row_off(valid ? key : k_lo) + g * 8;
+            const size_t src = (slice_pages ? slice_off + (size_t)(valid ? kr : 0) * D
+                                            : row_off(valid ? key : k_lo)) + g * 8;
             cp_async_16(sk + swz<D>(kr, g), a.k + src, valid ? 16u : 0u);
             cp_async_16(sv + swz<D>(kr, g), a.v + src, valid ? 16u : 0u);
         }
@@ -321,8 +331,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs a)
     int k_last = L - 1;
     if (a.causal) k_last = min(k_last, i + L - a.Sq);
     const int k_first = (a.window > 0) ? max(0, i + L - a.Sq - a.window + 1) : 0;
-    const int s_lo = k_first / a.chunk;
-    const int ns = (k_last >= k_first) ? (L + a.chunk - 1) / a.chunk : 0;
+    // the splits start at the sequence's first visible key, rounded down to a
+    // multiple of 64 (see the split kernel)
+    const int k_base = (a.window > 0) ? (max(0, L - a.Sq - a.window + 1) & ~63) : 0;
+    const int s_lo = (k_first - k_base) / a.chunk;
+    const int ns = (k_last >= k_first) ? (L - k_base + a.chunk - 1) / a.chunk : 0;
     const size_t stride = (size_t)a.B * a.Hq * a.Sq;
     const float sg = (a.sinks != nullptr) ? a.sinks[h] * kLog2ef : -INFINITY;
     float M = sg;
