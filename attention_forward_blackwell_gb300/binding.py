@@ -34,6 +34,8 @@ SIGNATURES = {
                                  _I, _F, _I, _VP]),
     "fa_fwd_prefill_varlen": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I,
                                    _I, _F, _I, _I, _VP, _VP]),
+    "fa_fwd_prefill_varlen_paged": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I,
+                                         _I, _I, _I, _I, _I, _F, _I, _I, _VP, _VP]),
     "fa_fwd_decode": (_I, _FWD + [_VP]),
     "fa_fwd_decode_splits": (_I, _FWD + [_I, _VP]),
     "fa_fwd_decode_noalloc": (_I, _FWD + [_VP]),
@@ -244,6 +246,53 @@ def prefill_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
                                      _stream_ptr(stream))
     if st != FA_OK:
         raise FaError(st, "fa_fwd_prefill_varlen")
+    return out, lse
+
+
+def prefill_varlen_paged(q, k_cache, v_cache, cu_seqlens_q, max_seqlen_q, block_table, seqlens_k,
+                         scale=None, causal=False, window=0, sinks=None, out=None, lse=None,
+                         stream=None):
+    """Packed queries q [total_q, Hq, d] (offsets cu_seqlens_q [B + 1]) over
+    paged caches [num_pages, Hkv, page_size, d] (block_table [B, max_pages],
+    seqlens_k [B]) through ``fa_fwd_prefill_varlen_paged``; returns
+    o [total_q, Hq, d] and lse [Hq, total_q]."""
+    if not q.is_cuda or q.dtype != torch.bfloat16 or q.dim() != 3:
+        raise ValueError("q must be a CUDA bf16 tensor [tokens, heads, d]")
+    if (k_cache.shape != v_cache.shape or k_cache.dim() != 4 or not k_cache.is_cuda
+            or k_cache.dtype != torch.bfloat16 or v_cache.dtype != torch.bfloat16):
+        raise ValueError("caches must be CUDA bf16 tensors [num_pages, Hkv, page_size, d]")
+    total_q, Hq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_cache.shape
+    if dk != d:
+        raise ValueError("head dims differ")
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (seqlens_k, "seqlens_k")):
+        if not t.is_cuda or t.dtype != torch.int32 or t.dim() != 1:
+            raise ValueError(f"{n} must be a CUDA int32 vector")
+    B = cu_seqlens_q.numel() - 1
+    if seqlens_k.shape != (B,):
+        raise ValueError("seqlens_k must be [B] with B + 1 query offsets")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError("block_table must be int32 [B, max_pages]")
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    cu_seqlens_q, seqlens_k = cu_seqlens_q.contiguous(), seqlens_k.contiguous()
+    block_table = block_table.contiguous()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(Hq, total_q, device=q.device, dtype=torch.float32)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (Hq, total_q) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 tensor [Hq, total_q]")
+    sinks = _check_sinks(sinks, Hq)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    st = lib().fa_fwd_prefill_varlen_paged(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+        _ptr(seqlens_k), _ptr(block_table), block_table.shape[1], page_size, num_pages, B,
+        int(max_seqlen_q), total_q, Hq, Hkv, d, scale, int(bool(causal)), int(window),
+        _ptr(sinks), _stream_ptr(stream))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_prefill_varlen_paged")
     return out, lse
 
 

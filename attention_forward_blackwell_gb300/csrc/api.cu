@@ -255,7 +255,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     if (!di) return FA_ERR_CUDA;
     if (!di->supported) return FA_ERR_UNSUPPORTED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (sk == 0 || (vl && vl->total_k == 0)) {
+    if (sk == 0 || (vl && !block_table && vl->total_k == 0)) {
         // no keys anywhere: O = 0 and LSE = -inf (or the sink); for packed
         // sequences, O [total_q, hq, d] and LSE [hq, total_q] read as one
         // sequence of total_q rows
@@ -265,22 +265,28 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     }
     PrefillLaunch p{};
     const unsigned long long row_bytes = (unsigned long long)head_dim * 2;
+    // Q, O: token-major packed tensors (map {d, tokens, heads}, a token's
+    // heads adjacent) or dense [B, Hq, Sq, d]; K, V: paged caches, packed or
+    // dense
     if (vl) {
-        // token-major packed tensors: map {d, tokens, heads}, a token's heads adjacent
         if (!encode_map_strided(&p.tm_q, q, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes) ||
-            !encode_map_strided(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
-            !encode_map_strided(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
             !encode_map_strided(&p.tm_o, o, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes))
             return FA_ERR_INVALID_ARG;
-    } else {
-        const int kv_rows = block_table ? page_size : sk;
-        const long long kv_planes =
-            block_table ? (long long)num_pages * hkv : (long long)batch * hkv;
-        if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
-            !encode_map(&p.tm_k, k, head_dim, kv_rows, kv_planes) ||
-            !encode_map(&p.tm_v, v, head_dim, kv_rows, kv_planes) ||
-            !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq))
+    } else if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
+               !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq)) {
+        return FA_ERR_INVALID_ARG;
+    }
+    if (block_table) {
+        if (!encode_map(&p.tm_k, k, head_dim, page_size, (long long)num_pages * hkv) ||
+            !encode_map(&p.tm_v, v, head_dim, page_size, (long long)num_pages * hkv))
             return FA_ERR_INVALID_ARG;
+    } else if (vl) {
+        if (!encode_map_strided(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
+            !encode_map_strided(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes))
+            return FA_ERR_INVALID_ARG;
+    } else if (!encode_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv) ||
+               !encode_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv)) {
+        return FA_ERR_INVALID_ARG;
     }
     PrefillArgs& a = p.args;
     if (vl) {
@@ -404,6 +410,28 @@ fa_status fa_fwd_prefill_varlen(const void* q, const void* k, const void* v, voi
     return prefill_impl(q, k, v, o, lse, batch, hq, hkv, max_seqlen_q,
                         total_k > 0 ? max_seqlen_k : 0, nullptr, head_dim, scale, causal, window,
                         sinks, nullptr, 0, 0, 0, stream, &vl);
+}
+
+fa_status fa_fwd_prefill_varlen_paged(const void* q, const void* k_cache, const void* v_cache,
+                                      void* o, float* lse, const int* cu_seqlens_q,
+                                      const int* seqlens_k, const int* block_table,
+                                      int max_pages, int page_size, int num_pages, int batch,
+                                      int max_seqlen_q, int total_q, int hq, int hkv,
+                                      int head_dim, float scale, int causal, int window,
+                                      const float* sinks, fa_stream_t stream) {
+    if (batch < 0 || max_seqlen_q < 0 || total_q < 0) return FA_ERR_INVALID_ARG;
+    if (batch == 0 || total_q == 0 || hq == 0) return FA_OK;   // nothing to compute
+    if (max_seqlen_q == 0 || !cu_seqlens_q) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) != 0) return FA_ERR_MISALIGNED;
+    fa_status st = check_paged(seqlens_k, block_table, max_pages, page_size, num_pages, batch, hq,
+                               max_seqlen_q);
+    if (st != FA_OK) return st;
+    if (page_size % 128 != 0) return FA_ERR_UNSUPPORTED;   // a key tile must fit a page
+    if ((long long)total_q * hq * head_dim >= (1ll << 40)) return FA_ERR_INVALID_ARG;
+    const Varlen vl{cu_seqlens_q, nullptr, total_q, 0};
+    return prefill_impl(q, k_cache, v_cache, o, lse, batch, hq, hkv, max_seqlen_q,
+                        max_pages * page_size, seqlens_k, head_dim, scale, causal, window, sinks,
+                        block_table, max_pages, page_size, num_pages, stream, &vl);
 }
 
 fa_status fa_fwd_decode(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -37,7 +37,8 @@ struct PrefillArgs {
     int page_size;
     // Packed variable-length sequences (nullptr: dense): sequence b owns
     // query tokens [cu_seqlens_q[b], cu_seqlens_q[b+1]) of Q, O [total_q, Hq, d]
-    // and keys [cu_seqlens_k[b], cu_seqlens_k[b+1]) of K, V [total_k, Hkv, d];
+    // and keys [cu_seqlens_k[b], cu_seqlens_k[b+1]) of K, V [total_k, Hkv, d]
+    // (with paged caches instead: seqlens_k[b] keys through the block table);
     // LSE is [Hq, total_q].  Offsets are clamped to [0, total] in the kernel.
     // Sq is then the largest query length (units per (b, h) = num_mblk).
     const int* cu_seqlens_q;

@@ -228,12 +228,18 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a, int c)
         // the packed tensors
         const int qs = min(max(a.cu_seqlens_q[w.b], 0), a.total_q);
         const int qe = min(max(a.cu_seqlens_q[w.b + 1], qs), a.total_q);
-        const int ks = min(max(a.cu_seqlens_k[w.b], 0), a.total_k);
-        const int ke = min(max(a.cu_seqlens_k[w.b + 1], ks), a.total_k);
         w.q0 = qs;
-        w.k0 = ks;
         w.Lq = qe - qs;
-        L = ke - ks;
+        if (a.block_table != nullptr) {
+            // keys in paged caches: per-sequence lengths, rows by page
+            L = max(0, min(a.seqlens_k[w.b], a.Sk));
+            w.k0 = 0;
+        } else {
+            const int ks = min(max(a.cu_seqlens_k[w.b], 0), a.total_k);
+            const int ke = min(max(a.cu_seqlens_k[w.b + 1], ks), a.total_k);
+            w.k0 = ks;
+            L = ke - ks;
+        }
         w.off = L - w.Lq;
     } else {
         // (Lq, q0, k0 are read by the packed-sequence kernels only)

@@ -51,10 +51,10 @@ CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
     "prefill": ("e67ed15139b168cca1d6f28d33f98e41b00346ee1a7e8f5af7913cf42f021a24",
                 118334976, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (464.13 MB) and scaled to batch 64 by the
+    # captured at batch 16 (463.87 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
-    "decode": ("c3984c96d483e09007206d223eb17d584e4da8584d32db373e192416e68b34e6",
-               2207660607, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    "decode": ("ad2a200dae3f194bb625da169552e109cd1851933861a5bd158c043234c1681f",
+               2206446577, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 

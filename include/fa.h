@@ -190,6 +190,26 @@ fa_status fa_fwd_prefill_varlen(const void *q, const void *k, const void *v, voi
                                 fa_stream_t stream);
 
 /*
+ * Packed queries over paged K/V caches: the queries, O and LSE of
+ * fa_fwd_prefill_varlen (q, o [total_q, hq, head_dim], lse [hq, total_q],
+ * cu_seqlens_q [batch + 1]) with the keys of fa_fwd_prefill_paged (k_cache,
+ * v_cache [num_pages, hkv, page_size, head_dim], block_table
+ * [batch, max_pages], seqlens_k [batch] required, page_size a multiple of
+ * 128).  Sequence b's query token t (0-based within the sequence) is row
+ * t + seqlens_k[b] - Lq_b of the causal alignment, as everywhere: the typical
+ * use is a chunk of new tokens whose keys, together with the earlier ones,
+ * are already in the caches.  Same window, sink and error rules as the two
+ * calls it combines.
+ */
+fa_status fa_fwd_prefill_varlen_paged(const void *q, const void *k_cache, const void *v_cache,
+                                      void *o, float *lse, const int *cu_seqlens_q,
+                                      const int *seqlens_k, const int *block_table,
+                                      int max_pages, int page_size, int num_pages, int batch,
+                                      int max_seqlen_q, int total_q, int hq, int hkv,
+                                      int head_dim, float scale, int causal, int window,
+                                      const float *sinks, fa_stream_t stream);
+
+/*
  * Decode with a sliding window and/or attention sinks: the same window and
  * sink semantics as fa_fwd_prefill_ex (for sq = 1 the window keeps the last
  * `window` keys of each sequence).  Splits wholly below a row's window are

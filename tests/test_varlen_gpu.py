@@ -137,3 +137,49 @@ def test_prefill_varlen_offsets_clamped_and_args():
     good = torch.tensor([0, 100, 200], dtype=torch.int32, device="cuda")
     with pytest.raises(binding.FaError):   # max_seqlen_q = 0 with tokens present
         binding.prefill_varlen(q, k, v, good, good, 0, 100)
+
+
+PAGED_CASES = [
+    # Hq, Hkv, d, page_size, lens_q, lens_k, causal
+    (4, 2, 128, 128, [100, 257, 1], [600, 257, 900], True),   # chunks of new tokens
+    (2, 2, 64, 256, [300, 50], [300, 1000], False),
+    (4, 1, 256, 128, [129, 64], [400, 64], True),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,P,lens_q,lens_k,causal", PAGED_CASES,
+                         ids=[f"h{c[0]}x{c[1]}d{c[2]}p{c[3]}{'c' if c[6] else 'n'}"
+                              for c in PAGED_CASES])
+def test_prefill_varlen_paged(Hq, Hkv, d, P, lens_q, lens_k, causal):
+    """Packed queries over shuffled, NaN-poisoned pages: each sequence against
+    the oracle, and bit for bit against the packed-key path on the same keys."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    from test_paged_gpu import to_pages
+    q, k, v, cq, ck = packed(lens_q, lens_k, Hq, Hkv, d, seed=7 * P + d)
+    B, Sk = len(lens_k), max(lens_k)
+    ks = np.concatenate([[0], np.cumsum(lens_k)])
+    kd = torch.zeros(B, Hkv, Sk, d, device="cuda", dtype=torch.bfloat16)
+    vd = torch.zeros_like(kd)
+    for b in range(B):
+        kd[b, :, :lens_k[b]] = k[ks[b]:ks[b + 1]].permute(1, 0, 2)
+        vd[b, :, :lens_k[b]] = v[ks[b]:ks[b + 1]].permute(1, 0, 2)
+    kc, vc, table, _ = to_pages(kd, vd, lens_k, P, seed=P + d)
+    lens_t = torch.tensor(lens_k, dtype=torch.int32, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill_varlen_paged(q, kc, vc, cq, max(lens_q), table, lens_t, scale=scale,
+                                          causal=causal)
+    torch.cuda.synchronize()
+    check_device_error()
+    o2, l2 = binding.prefill_varlen(q, k, v, cq, ck, max(lens_q), max(lens_k), scale=scale,
+                                    causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    qs = np.concatenate([[0], np.cumsum(lens_q)])
+    for b in range(B):
+        qb, kb, vb = seq(q, qs[b], qs[b + 1]), seq(k, ks[b], ks[b + 1]), seq(v, ks[b], ks[b + 1])
+        ro, rl = oracle.attention_fwd(inputs.bf16_bits(qb), inputs.bf16_bits(kb),
+                                      inputs.bf16_bits(vb), scale=scale, causal=causal,
+                                      threads=THREADS)
+        compare(seq(o, qs[b], qs[b + 1]), lse[:, qs[b]:qs[b + 1]].unsqueeze(0), ro, rl,
+                f"varlen paged seq {b}")
+    free_cuda()
