@@ -108,6 +108,24 @@ def test_paged_host_validation(lib):
     assert lib.fa_fwd_decode_paged(*(ok[:13] + (0,) + ok[14:]), None) == 1   # no pages
 
 
+def test_varlen_paged_host_validation(lib):
+    # (q, kc, vc, o, lse, cu_q, seqlens, table, max_pages, page, pages, B, max_q, total_q,
+    #  Hq, Hkv, d, scale, causal, window, sinks)
+    ok = [P16, P16, P16, P16, P16, P16, P16, P16, 2, 128, 4, 1, 8, 8, 2, 1, 64, 1.0, 0, 0, None]
+    def call(**kw):
+        a = list(ok)
+        for i, val in kw.items():
+            a[int(i[1:])] = val
+        return lib.fa_fwd_prefill_varlen_paged(*a, None)
+    assert call(a5=None) == 1              # no query offsets
+    assert call(a6=None) == 1              # no key lengths
+    assert call(a7=None) == 1              # no block table
+    assert call(a9=100) == 2               # a key tile must fit a page
+    assert call(a12=0) == 1                # max_seqlen_q = 0 with tokens present
+    assert call(a5=P_MIS4) == 3            # misaligned offsets
+    assert call(a11=0, a13=0) == 0         # nothing to compute
+
+
 def test_binding_rejects_bad_tensors():
     import torch
     from attention_forward_blackwell_gb300 import binding
