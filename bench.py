@@ -49,8 +49,8 @@ KERNEL_SOURCES = {
 }
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("e67ed15139b168cca1d6f28d33f98e41b00346ee1a7e8f5af7913cf42f021a24",
-                118334976, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    "prefill": ("5bed0a549fc3444a7e7947f8922e79e770a402c95d9b3ea0c079edc80ed110db",
+                120160768, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
     # captured at batch 16 (463.87 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
     "decode": ("ad2a200dae3f194bb625da169552e109cd1851933861a5bd158c043234c1681f",
@@ -87,6 +87,9 @@ def parse_args(argv=None):
                         "smaller batch keeps profiler captures small")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU (oracle) baseline sample")
+    p.add_argument("--only", default=None, metavar="WORKLOAD",
+                   help="time one named prefill workload alone (e.g. for a profiler "
+                        "capture of its kernel) and print its median; not the bench line")
     return p.parse_args(argv)
 
 
@@ -524,11 +527,51 @@ def run_reference(args, dist):
     }
 
 
+def run_only(args, dist):
+    """One prefill workload (workloads.ALL by name), L2 flushed before each of
+    `steps` timed launches after `warmup` untimed ones."""
+    import torch
+    from attention_forward_blackwell_gb300 import binding, build, inputs, workloads as W
+
+    build.build()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    w = {x.name: x for x in W.ALL}.get(args.only)
+    if w is None or w.Sq != w.Sk:
+        raise SystemExit(f"--only: not a prefill workload: {args.only}")
+    x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device=dev,
+                           k_scale=w.k_scale)
+    o = torch.empty_like(x.q)
+    lse = torch.empty(w.B, w.Hq, w.Sq, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.int8, device=dev)
+
+    def step():
+        binding.prefill(x.q, x.k, x.v, scale=w.scale, causal=w.causal, out=o, lse=lse)
+
+    for _ in range(max(1, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    ev = _events(torch, args.steps)
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    assert binding.get_device_error() == binding.FA_OK
+    ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+    f = W.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.d, w.causal)
+    return {"only": w.name, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 2)}
+
+
 def main(argv=None):
     args = parse_args(argv)
     dist = Dist(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.only is not None:
+            res = run_only(args, dist)
+        elif args.impl == "reference":
             res = run_reference(args, dist)
         else:
             res = run_ours(args, dist)
