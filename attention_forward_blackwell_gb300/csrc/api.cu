@@ -572,6 +572,6 @@ fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim,
     return FA_OK;
 }
 
-int fa_version(void) { return 110; }
+int fa_version(void) { return 200; }
 
 }  // extern "C"
