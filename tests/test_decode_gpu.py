@@ -98,3 +98,21 @@ def test_full_decode_configuration_all_rows():
     compare(o, lse, ro, rl, "decode full config")
     del x
     free_cuda()
+
+
+def test_decode_many_sequences_max_queries_sampled():
+    """256 sequences, 16 queries each (the decode maximum), GQA 4, lengths
+    U[1, 2000] with poisoned padding: sampled rows against the oracle."""
+    from attention_forward_blackwell_gb300 import inputs
+    B, Hq, Hkv, Sq, Sk, d = 256, 16, 4, 16, 2000, 128
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=640, device="cuda", lengths=(1, Sk))
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    o, lse = _decode(x, 1 / math.sqrt(d), True)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([np.arange(64), rng.integers(0, B * Hq * Sq, 400),
+                                     np.arange(B * Hq * Sq - 64, B * Hq * Sq)]))
+    ro, rl = oracle_for(x, 1 / math.sqrt(d), True, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, "decode B=256 Sq=16 (sampled)")
+    free_cuda()

@@ -266,3 +266,22 @@ def test_split_units_replay_in_a_cuda_graph():
         torch.cuda.synchronize()
         check_device_error()
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,d,causal", [
+    (1, 128, 8, 300, 128, True),      # many heads: 128 x 2 units
+    (64, 2, 1, 129, 64, False),       # many tiny sequences: 128 units of 129 rows
+])
+def test_wide_grids(B, Hq, Hkv, S, d, causal):
+    """Grids of many small units (every unit boundary case at once)."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(B, Hq, Hkv, S, S, d, tag=660 + Hq, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    check_device_error()
+    rows = sample_rows(B, Hq, S, n_random=600, seed=B + Hq)
+    ro, rl = oracle_for(x, scale, causal, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, f"wide grid {B, Hq, Hkv, S, d}")
+    free_cuda()
