@@ -16,8 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libfa_gb300.so")
-SOURCES = ["prefill_d128.cu", "prefill_d256.cu", "prefill_d96.cu", "prefill_d64.cu",
-           "decode.cu", "selftest.cu", "api.cu", "decode_noalloc.cu"]
+SOURCES = ["prefill_d512.cu", "prefill_d128.cu", "prefill_d256.cu", "prefill_d96.cu",
+           "prefill_d64.cu", "decode.cu", "selftest.cu", "api.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", CSRC, "-I", INCLUDE]

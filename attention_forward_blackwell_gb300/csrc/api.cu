@@ -249,8 +249,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     fa_status st = check_common(q, k, v, o, lse, batch, hq, hkv, sq, sk, scale, c);
     if (st != FA_OK || c.noop) return st;
     if ((reinterpret_cast<uintptr_t>(sinks) & 3u) != 0) return FA_ERR_MISALIGNED;
-    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
-        return FA_ERR_UNSUPPORTED;
+    if (!prefill_head_dim_ok(head_dim)) return FA_ERR_UNSUPPORTED;
     const DeviceInfo* di = device_info();
     if (!di) return FA_ERR_CUDA;
     if (!di->supported) return FA_ERR_UNSUPPORTED;
@@ -320,12 +319,14 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     p.causal = causal ? 1 : 0;
     // work split: whole units, then the last partial wave's units in pieces
     const long long units = (long long)batch * hq * a.num_mblk;
-    if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    if (units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
     a.nk = (sk + 127) / 128;
     // (a windowed unit has fewer key blocks than nk: it is not split either)
     // (packed sequences have units of different lengths: not split either)
+    // (head_dim 512 runs two CTAs per unit already: not split either)
     const PrefillPlan plan =
-        plan_prefill(units, a.nk, p.causal || a.window > 0 || vl != nullptr, di->num_sms);
+        plan_prefill(units, a.nk, p.causal || a.window > 0 || vl != nullptr || head_dim == 512,
+                     di->num_sms);
     a.n_full = plan.n_full;
     a.split = plan.split;
     p.n_tail = plan.n_tail;
@@ -348,7 +349,8 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
         case 64: e = launch_prefill_d64(p, s); break;
         case 96: e = launch_prefill_d96(p, s); break;
         case 128: e = launch_prefill_d128(p, s); break;
-        default: e = launch_prefill_d256(p, s); break;
+        case 256: e = launch_prefill_d256(p, s); break;
+        default: e = launch_prefill_d512(p, s); break;
     }
     if (ws != nullptr && cudaFreeAsync(ws, s) != cudaSuccess) return FA_ERR_CUDA;
     return from_cuda(e);
@@ -560,12 +562,12 @@ fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim,
     if (!out || batch <= 0 || hq <= 0 || sq <= 0 || sk <= 0 || batch > 65535 || hq > 65535 ||
         num_sms < 1)
         return FA_ERR_INVALID_ARG;
-    if (head_dim != 64 && head_dim != 96 && head_dim != 128 && head_dim != 256)
-        return FA_ERR_INVALID_ARG;
+    if (!prefill_head_dim_ok(head_dim)) return FA_ERR_INVALID_ARG;
     const int rows = prefill_rows_per_cta(head_dim);
     const long long units = (long long)batch * hq * ((sq + rows - 1) / rows);
-    if (units >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-    const PrefillPlan p = plan_prefill(units, (sk + 127) / 128, causal ? 1 : 0, num_sms);
+    if (units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    const PrefillPlan p =
+        plan_prefill(units, (sk + 127) / 128, (causal || head_dim == 512) ? 1 : 0, num_sms);
     out[0] = p.n_full;
     out[1] = p.n_tail;
     out[2] = p.split;

@@ -86,6 +86,13 @@ struct PrefillLaunch {
 
 // Query rows of one prefill unit (query block) for a head dimension.
 inline int prefill_rows_per_cta(int head_dim) { return head_dim <= 128 ? 256 : 128; }
+// CTAs per unit: head_dim 512 shares the output columns out over two.
+inline int prefill_ctas_per_unit(int head_dim) { return head_dim == 512 ? 2 : 1; }
+// Head dimensions of the prefill kernels.
+inline bool prefill_head_dim_ok(int head_dim) {
+    return head_dim == 64 || head_dim == 96 || head_dim == 128 || head_dim == 256 ||
+           head_dim == 512;
+}
 
 // Split of the prefill work over the grid.  With units of equal work
 // (non-causal), the units beyond the last full wave of `ctas` whole-unit
@@ -121,6 +128,7 @@ cudaError_t launch_prefill_d64(const PrefillLaunch& p, cudaStream_t s);
 cudaError_t launch_prefill_d96(const PrefillLaunch& p, cudaStream_t s);
 cudaError_t launch_prefill_d128(const PrefillLaunch& p, cudaStream_t s);
 cudaError_t launch_prefill_d256(const PrefillLaunch& p, cudaStream_t s);
+cudaError_t launch_prefill_d512(const PrefillLaunch& p, cudaStream_t s);
 
 // ------------------------------------------------------------ decode ----
 

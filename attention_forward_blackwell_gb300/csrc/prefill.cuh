@@ -76,15 +76,24 @@ struct PrefillTraits {
     static constexpr int NCH = (D + 63) / 64;          // 64-element (128-byte) row chunks
     static constexpr int CHUNK = 128 * 128;            // one chunk of 128 rows, bytes
     static constexpr int QTILE = NCH * CHUNK;
-    static constexpr int SLOT_CH = (NCH >= 2) ? 2 : 1; // chunks per ring slot
-    static constexpr int PIECES = NCH / SLOT_CH;       // ring slots per K or V tile
+    // head_dim 512: the output columns are shared out over DV_SPLIT = 2 CTAs
+    // per Q tile (each computes the full scores and one 256-column half of
+    // O), because 512 fp32 O columns leave no tensor memory for the scores.
+    static constexpr int DV_SPLIT = (D == 512) ? 2 : 1;
+    static constexpr int D_COLS = D / DV_SPLIT;        // O accumulator columns of a CTA
+    static constexpr int OCH = (D_COLS + 63) / 64;     // 64-column chunks of a CTA's O
+    // chunks per ring slot: one at head_dim 512 (the 128 KB Q tile leaves
+    // room for five 16 KB slots only)
+    static constexpr int SLOT_CH = (D == 512) ? 1 : ((NCH >= 2) ? 2 : 1);
+    static constexpr int PIECES = NCH / SLOT_CH;       // ring slots per K tile
+    static constexpr int VPIECES = OCH / SLOT_CH;      // ring slots per (own part of a) V tile
     static constexpr int SLOT = SLOT_CH * CHUNK;
-    static constexpr int NSLOT = (D == 64) ? 8 : 4;
+    static constexpr int NSLOT = (D == 64) ? 8 : ((D == 512) ? 5 : 4);
     static constexpr int KSTEPS = D / 16;              // score MMA steps of K = 16
-    static constexpr int D_COLS = D;                   // O accumulator columns
     // Value MMA N per instruction (head_dim 96: N = 96, i.e. one full and one
-    // half 64-column chunk of the MN-major V tile).
-    static constexpr int PV_N = (D <= 128) ? D : 128;
+    // half 64-column chunk of the MN-major V tile; head_dim 512: one 64-column
+    // chunk, the content of one ring slot).
+    static constexpr int PV_N = (D <= 128) ? D : ((D == 512) ? 64 : 128);
     static constexpr int NUM_WARPS = (NQ + 2) * 4;
     static constexpr int THREADS = NUM_WARPS * 32;
     static constexpr int CORR_WG = NQ;
@@ -114,6 +123,9 @@ struct PrefillTraits {
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
     static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX;
+    static_assert(DV_SPLIT == 1 ? VPIECES == PIECES : NQ == 1,
+                  "split output columns only with one Q tile per CTA");
+    static_assert(SMEM_TOTAL <= 232448, "shared memory per CTA exceeds the sm_103 limit");
 
     __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * 128); }
     __device__ static constexpr uint32_t o_col(int t) {
@@ -170,7 +182,10 @@ __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int
 
 // Per-CTA work coordinates, computed identically by every thread.
 //
-// The grid is one-dimensional.  Its first n_full CTAs each process a whole
+// The grid is one-dimensional.  With output columns split over DV_SPLIT CTAs
+// (head_dim 512), the CTA index's fastest digit selects the column part and
+// the rest is the unit index below (the parts of one unit run side by side
+// and share its Q, K and V through L2).  Its first n_full CTAs each process a whole
 // unit (batch entry, query head, query block), in the order query block
 // (fastest), head, batch entry; causal units in the order (batch entry, head)
 // fastest, then query block heaviest first.  The remaining
@@ -190,11 +205,17 @@ struct PrefillWork {
     // packed sequences only: query rows of the sequence, and its first query
     // token and first key token in the packed tensors
     int Lq, q0, k0;
+    int dv0;       // first output column of this CTA (0 unless DV_SPLIT > 1)
 };
 
 template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
 __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a, int c) {
     PrefillWork w;
+    w.dv0 = 0;
+    if constexpr (T::DV_SPLIT > 1) {
+        w.dv0 = (c % T::DV_SPLIT) * T::D_COLS;
+        c /= T::DV_SPLIT;
+    }
     int u, ke;
     if (c < a.n_full) {
         u = c;
@@ -607,6 +628,170 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     __syncwarp();
 }
 
+// ------------------------------------ split output columns (head_dim 512) ----
+//
+// With DV_SPLIT > 1 a CTA holds the whole 128 x 512 Q tile (128 KB) and
+// streams K and its own 256 columns of V through five one-chunk (16 KB) ring
+// slots.  The ring is filled in the order the MMA warp consumes it -- K_0,
+// then K_{j+1} before V_j -- because with one Q tile the score MMA of block
+// j+1 is issued before the value MMA of block j, and five slots cannot hold
+// a value tile while a whole key tile waits behind it.  Each K piece is
+// released as soon as its four K-steps have been issued and completed.
+
+// Producer: Q once, then the pieces in consumption order.
+template <class T, bool VARLEN>
+__device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                     const CUtensorMap* tm_v, const PrefillArgs& a,
+                                     const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
+                                     uint32_t sRing, const WaitCtx& wc) {
+    const int lane = threadIdx.x & 31;
+    if (w.n_max <= 0) return;
+    const uint32_t bar_q = smem_u32(&aux->bar_q);
+    if (lane == 0) {
+        tma_prefetch_desc(tm_q);
+        tma_prefetch_desc(tm_k);
+        tma_prefetch_desc(tm_v);
+        mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+            tma_load_3d(sQ + c * T::CHUNK, tm_q, c * 64, (VARLEN ? w.q0 : 0) + w.row0,
+                        VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
+    }
+    int p = 0;   // ring position of the next piece
+    // one 64-column chunk of K_j (is_v = false) or of this CTA's part of V_j
+    auto load = [&](int j, bool is_v, int pc) -> bool {
+        const uint32_t slot = ring_slot<T>(p);
+        if (!mbar_wait(smem_u32(&aux->bar_empty[slot]), ring_phase<T>(p) ^ 1u, wc,
+                       kErrWaitTimeout | kSiteLoadEmpty))
+            return false;
+        const uint32_t full = smem_u32(&aux->bar_full[slot]);
+        const uint32_t dst = sRing + slot * T::SLOT;
+        const int jk = w.kb + j;
+        const int rv = w.L - jk * T::BN;
+        int ty = (VARLEN ? w.k0 : 0) + jk * T::BN, tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
+        if (a.block_table != nullptr) {
+            const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
+            ty = ty % a.page_size;
+            tz = page * a.Hkv + w.hk;
+        }
+        const int x = pc * 64 + (is_v ? w.dv0 : 0);
+        if (is_v && j == w.n_max - 1 && rv < T::BN) {
+            // partial last value tile: rows [rv, BN) zeroed before publication
+            const uint32_t tail = smem_u32(&aux->bar_tail);
+            if (lane == 0) {
+                mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
+                tma_load_3d(dst, tm_v, x, ty, tz, tail);
+            }
+            if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail))
+                return false;
+            zero_value_tail<T>(dst, rv);
+            if (lane == 0) mbar_arrive(full);
+        } else if (lane == 0) {
+            mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
+            tma_load_3d(dst, is_v ? tm_v : tm_k, x, ty, tz, full);
+        }
+        __syncwarp();
+        ++p;
+        return true;
+    };
+    bool ok = true;
+    for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(0, false, pc);
+    for (int j = 0; j < w.n_max && ok; ++j) {
+        if (j + 1 < w.n_max)
+            for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(j + 1, false, pc);
+        for (int pc = 0; pc < T::VPIECES && ok; ++pc) ok = load(j, true, pc);
+    }
+    // every copy issued must have landed before the CTA exits
+    if (lane == 0) {
+        mbar_wait_drain(bar_q, 0, a.wait_limit_ns);
+        for (int q = p > T::NSLOT ? p - T::NSLOT : 0; q < p; ++q)
+            mbar_wait_drain(smem_u32(&aux->bar_full[ring_slot<T>(q)]), ring_phase<T>(q),
+                            a.wait_limit_ns);
+    }
+    __syncwarp();
+}
+
+// MMA issue (one lane): S(0); then per block j: S(j+1) into the other score
+// buffer (once PV(j-1), which read that buffer's P, has completed), and
+// PV(j) over the CTA's output columns, one N = 64 chunk per ring piece.
+template <class T>
+__device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
+                                    PrefillAux<T>* aux, uint32_t tmem, uint32_t sQ,
+                                    uint32_t sRing, const WaitCtx& wc) {
+    const int lane = threadIdx.x & 31;
+    if (lane != 0) {
+        __syncwarp();
+        return;
+    }
+    const uint32_t qd0 = sdesc_lo_sw128(sQ, 16);
+    const uint32_t kd0 = sdesc_lo_sw128(sRing, 16);
+    const uint32_t vd0 = sdesc_lo_sw128(sRing, T::CHUNK);
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
+    int p = 0;   // ring position of the next piece (the producer's order)
+    auto next_piece = [&](unsigned site) -> bool {
+        if (!mbar_wait_lane(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
+                            kErrWaitTimeout | site))
+            return false;
+        tc_fence_after();
+        return true;
+    };
+    auto slot_desc = [&](uint32_t d0) { return d0 + (uint32_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
+    // S(buffer sb) = Q K^T, each K piece released once its K-steps complete
+    auto score = [&](int sb) -> bool {
+        for (int pc = 0; pc < T::PIECES; ++pc) {
+            if (!next_piece(kSiteMmaK)) return false;
+            const uint32_t kd = slot_desc(kd0);
+#pragma unroll
+            for (int kin = 0; kin < 4; ++kin) {
+                const int kk = pc * 4 + kin;
+                umma_ss_lo(tmem + T::s_col(sb), qd0 + kstep_off(kk), kd + kstep_off(kin), idesc_s,
+                           kk > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
+            ++p;
+        }
+        tc_commit(smem_u32(&aux->bar_s_full[sb]));
+        return true;
+    };
+    if (w.n_max > 0) do {
+        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        tc_fence_after();
+        if (!score(0)) break;
+        bool ok = true;
+        for (int j = 0; j < w.n_max && ok; ++j) {
+            if (j + 1 < w.n_max) {
+                if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                                              sig_par<T>(j - 1), wc, kErrWaitTimeout | kSiteMmaPv))
+                    break;
+                tc_fence_after();
+                if (!score((j + 1) & 1)) break;
+            }
+            if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
+                                kErrWaitTimeout | kSiteMmaP))
+                break;
+            tc_fence_after();
+            for (int nh = 0; nh < T::VPIECES; ++nh) {
+                if (!next_piece(kSiteMmaV)) {
+                    ok = false;
+                    break;
+                }
+                issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(j & 1) + 64,
+                               slot_desc(vd0), idesc_v, j == 0);
+                tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
+                ++p;
+            }
+            if (ok) tc_commit(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j)]));
+        }
+    } while (0);
+    {
+        const uint32_t drain = smem_u32(&aux->bar_drain[0]);
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0, a.wait_limit_ns);
+    }
+    __syncwarp();
+}
+
 // ------------------------------------------------------------- softmax ----
 
 template <class T, bool CAUSAL, bool WINDOW>
@@ -850,13 +1035,13 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
         uint4* dst = reinterpret_cast<uint4*>(
             a.o + (((size_t)b * a.Hq + h) * a.Sq + row) * T::D_COLS + c16 * 16);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int g8 = 0; g8 < 2; ++g8) {
             uint4 v;
-            v.x = pack_bf16x2(acc[8 * h + 0] * inv_l, acc[8 * h + 1] * inv_l);
-            v.y = pack_bf16x2(acc[8 * h + 2] * inv_l, acc[8 * h + 3] * inv_l);
-            v.z = pack_bf16x2(acc[8 * h + 4] * inv_l, acc[8 * h + 5] * inv_l);
-            v.w = pack_bf16x2(acc[8 * h + 6] * inv_l, acc[8 * h + 7] * inv_l);
-            dst[h] = v;
+            v.x = pack_bf16x2(acc[8 * g8 + 0] * inv_l, acc[8 * g8 + 1] * inv_l);
+            v.y = pack_bf16x2(acc[8 * g8 + 2] * inv_l, acc[8 * g8 + 3] * inv_l);
+            v.z = pack_bf16x2(acc[8 * g8 + 4] * inv_l, acc[8 * g8 + 5] * inv_l);
+            v.w = pack_bf16x2(acc[8 * g8 + 6] * inv_l, acc[8 * g8 + 7] * inv_l);
+            dst[g8] = v;
         }
         if (c16 == 0)
             a.lse[((size_t)b * a.Hq + h) * a.Sq + row] =
@@ -979,8 +1164,9 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         // packed sequences: a tile that runs past the end of its sequence is
         // stored row by row (a TMA store would write the next sequence's rows)
         const bool direct = VARLEN && w.row0 + t * T::BM + T::BM > w.Lq;
+        constexpr int d_full = T::D_COLS * T::DV_SPLIT;
         uint16_t* orow =
-            VARLEN ? a.o + ((size_t)(w.q0 + row) * a.Hq + w.h) * T::D_COLS : nullptr;
+            VARLEN ? a.o + ((size_t)(w.q0 + row) * a.Hq + w.h) * d_full + w.dv0 : nullptr;
 #pragma unroll 1
         for (int c32 = 0; c32 < (T::D_COLS + 31) / 32; ++c32) {
             uint32_t v[32];
@@ -1013,7 +1199,9 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                              : "memory");
             }
         }
-        if (row < (VARLEN ? w.Lq : a.Sq)) {
+        // (with split output columns every part has the same statistics;
+        // the first part stores LSE)
+        if (row < (VARLEN ? w.Lq : a.Sq) && (T::DV_SPLIT == 1 || w.dv0 == 0)) {
             const float lse = (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
             if constexpr (VARLEN)
                 a.lse[(size_t)w.h * a.total_q + w.q0 + row] = lse;   // [Hq, total_q]
@@ -1025,8 +1213,8 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         if (issuer && !direct && w.row0 + t * T::BM < (VARLEN ? w.Lq : a.Sq) &&
             mbar_wait_lane(smem_u32(&aux->bar_epi[t]), 0, wc, kErrWaitTimeout | kSiteEpiStage)) {
 #pragma unroll
-            for (int ch = 0; ch < T::NCH; ++ch)
-                tma_store_3d(tm_o, stage + ch * T::CHUNK, ch * 64,
+            for (int ch = 0; ch < T::OCH; ++ch)
+                tma_store_3d(tm_o, stage + ch * T::CHUNK, w.dv0 + ch * 64,
                              (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
                              VARLEN ? w.h : w.b * a.Hq + w.h);
             bulk_commit_group();
@@ -1101,15 +1289,22 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         prefill_softmax_role<T, CAUSAL, WINDOW>(wg, args, w, aux, tmem, wc, tr);
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
-        prefill_correction_role<T, !CAUSAL && !WINDOW && !VARLEN, VARLEN>(&tm_o, args, w, aux, tmem,
-                                                                          sQ, wc, tr);
+        prefill_correction_role<T, !CAUSAL && !WINDOW && !VARLEN && T::DV_SPLIT == 1, VARLEN>(
+            &tm_o, args, w, aux, tmem, sQ, wc, tr);
     } else {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
-        if (warp == T::MMA_WARP)
-            prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
-        else if (warp == T::LOAD_WARP)
-            prefill_load_role<T, CAUSAL, WINDOW, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ,
-                                                         sRing, wc, tr);
+        if constexpr (T::DV_SPLIT > 1) {
+            if (warp == T::MMA_WARP)
+                prefill_mma_role_dv<T>(args, w, aux, tmem, sQ, sRing, wc);
+            else if (warp == T::LOAD_WARP)
+                prefill_load_role_dv<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc);
+        } else {
+            if (warp == T::MMA_WARP)
+                prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
+            else if (warp == T::LOAD_WARP)
+                prefill_load_role<T, CAUSAL, WINDOW, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ,
+                                                             sRing, wc, tr);
+        }
     }
 
     tc_fence_before();
@@ -1119,7 +1314,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         tmem_dealloc(tmem, T::TMEM_COLS);
     }
     // the last piece of a split unit to arrive merges it, on all threads
-    if (!CAUSAL && !WINDOW && !VARLEN && aux->merge_last != 0 &&
+    if (!CAUSAL && !WINDOW && !VARLEN && T::DV_SPLIT == 1 && aux->merge_last != 0 &&
         ld_volatile_shared(wc.abort_flag) == 0)
         merge_unit<T>(args, aux->merge_unit[0], aux->merge_unit[1], aux->merge_unit[2],
                       aux->merge_unit[3], (int)threadIdx.x, T::THREADS);
@@ -1145,7 +1340,8 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          T::SMEM_TOTAL);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)p.args.n_full + (unsigned)p.n_tail * (unsigned)p.args.split;
+    const unsigned grid =
+        ((unsigned)p.args.n_full + (unsigned)p.n_tail * (unsigned)p.args.split) * T::DV_SPLIT;
     kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o, p.args);
     return cudaGetLastError();
 }

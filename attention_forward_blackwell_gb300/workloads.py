@@ -74,10 +74,18 @@ LONG_D96 = Workload("prefill_b2_h16_s4096_d96", 2, 16, 16, 4096, 4096, 96,
 GQA_D256 = Workload("causal_gqa_b4_hq32_hkv4_s2048_d256", 4, 32, 4, 2048, 2048,
                     256, True, 4, k_scale=0.5,
                     description="causal GQA B=4 Hq=32 Hkv=4 Sq=Sk=2048 d=256, K*0.5")
+# head_dim 512 (no configuration of the pages uses it): the FLOPs of the
+# 8K-key d=128 shape at a quarter of the heads times four the head dimension
+PREFILL_D512 = Workload("prefill_b2_h8_s4096_d512", 2, 8, 8, 4096, 4096, 512,
+                        False, 7,
+                        description="prefill MHA B=2 H=8 Sq=Sk=4096 d=512 non-causal")
+PREFILL_D512_CAUSAL = Workload("prefill_b2_h8_s4096_d512_causal", 2, 8, 8, 4096,
+                               4096, 512, True, 7,
+                               description="prefill MHA B=2 H=8 Sq=Sk=4096 d=512 causal")
 DECODE = Workload("decode_gqa_b64_hq64_hkv8_d128", 64, 64, 8, 1, 16384, 128,
                   False, 5, lengths=(1024, 16384), decode=True,
                   description="decode GQA B=64 Hq=64 Hkv=8 Sq=1 d=128, "
                               "L_b~U[1024,16384], KV padded to 16384")
 
 ALL = [TINY, PREFILL_D128, PREFILL_D128_CAUSAL, LONG_D128, LONG_D96, GQA_D256,
-       DECODE]
+       PREFILL_D512, PREFILL_D512_CAUSAL, DECODE]

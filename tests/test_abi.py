@@ -69,11 +69,31 @@ def test_host_validation(lib, fn, args, expect):
 
 
 def test_decode_specific_validation(lib):
-    # sq above the decode limit, and head_dim 96 (prefill only)
+    # sq above the decode limit, and head_dims 96 and 512 (prefill only)
     assert lib.fa_fwd_decode(P16, P16, P16, P16, P16, 1, 1, 1, 17, 8, None, 64, 1.0, 0,
                              None) == 1
     assert lib.fa_fwd_decode(P16, P16, P16, P16, P16, 1, 1, 1, 1, 8, None, 96, 1.0, 0,
                              None) == 2
+    assert lib.fa_fwd_decode(P16, P16, P16, P16, P16, 1, 1, 1, 1, 8, None, 512, 1.0, 0,
+                             None) == 2
+
+
+def test_prefill_head_dims(lib):
+    """head_dim 512 passes the prefill argument checks exactly as 64 does (on
+    a machine without the GPU both then stop at the same device check); head
+    dimensions outside {64, 96, 128, 256, 512} are rejected first."""
+    def call(d):
+        return lib.fa_fwd_prefill(P16, P16, P16, P16, P16, 1, 1, 1, 8, 8, None, d, 1.0, 0, None)
+    import torch
+    if not torch.cuda.is_available():   # (with a GPU the fake pointers would be read)
+        assert call(512) == call(64) != 2
+    for d in (384, 1024, 32, 80):
+        assert call(d) == 2
+    out = (ctypes.c_int * 3)()
+    # two CTAs per unit, never split along the keys
+    assert lib.fa_debug_prefill_plan(2, 8, 4096, 4096, 512, 0, 152, out) == 0
+    assert list(out) == [2 * 8 * 32, 0, 1]
+    assert lib.fa_debug_prefill_plan(2, 8, 4096, 4096, 384, 0, 152, out) == 1
 
 
 P_MIS4 = ctypes.c_void_p((1 << 12) + 2)   # not 4-byte aligned
