@@ -574,6 +574,6 @@ fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim,
     return FA_OK;
 }
 
-int fa_version(void) { return 200; }
+int fa_version(void) { return 300; }
 
 }  // extern "C"

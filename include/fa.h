@@ -58,8 +58,8 @@ typedef enum fa_status {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, hq % hkv != 0,
                                  bad scale, decode with sq > FA_DECODE_MAX_SQ */
-    FA_ERR_UNSUPPORTED = 2,   /* head_dim not 64/96/128/256 (prefill) or not
-                                 64/128/256 (decode); device not sm_103 */
+    FA_ERR_UNSUPPORTED = 2,   /* head_dim not 64/96/128/256/512 (prefill) or
+                                 not 64/128/256 (decode); device not sm_103 */
     FA_ERR_MISALIGNED = 3,    /* q, k, v or o not 16-byte aligned */
     FA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     FA_ERR_TIMEOUT = 5        /* a kernel wait ran out of time (device word) */
@@ -70,12 +70,15 @@ typedef enum fa_status {
 
 /*
  * Prefill forward.  Runs the warp-specialised tcgen05/TMEM kernel for
- * head_dim in {64, 96, 128, 256}: a TMA producer warp streams K/V tiles
+ * head_dim in {64, 96, 128, 256, 512}: a TMA producer warp streams K/V tiles
  * through an mbarrier ring, one warp issues the score MMA (S = Q K^T) and the
  * value MMA (O += P V) into tensor memory, softmax warpgroups turn S into P
  * with exp2, and a correction/epilogue warpgroup rebases O and writes O and
  * LSE ("b200-flash-attention4-planner", section A1 "Role example" and
- * section E steps 3-8).  One CTA per query block; for non-causal problems
+ * section E steps 3-8).  One CTA per query block (two at head_dim 512, each
+ * computing the scores over all 512 dimensions -- the head dimension's
+ * sub-tiles summed before the softmax, "STAGE_D.md" hd=512 -- and one
+ * 256-column half of O; LSE is stored by the first); for non-causal problems
  * the query blocks of the last, partial wave are split along the key axis
  * over several CTAs and merged on the device (see fa_debug_prefill_plan),
  * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
@@ -178,7 +181,7 @@ fa_status fa_fwd_decode_paged(const void *q, const void *k_cache, const void *v_
  * longer sequence beyond that are not written).  Offsets are clamped to
  * [0, total] on the device, so malformed offsets never address memory outside
  * the tensors.  Sequences without keys give O = 0 and LSE = -inf (or the
- * sink).  head_dim 64, 96, 128 or 256.  Returns FA_ERR_INVALID_ARG for
+ * sink).  head_dim 64, 96, 128, 256 or 512.  Returns FA_ERR_INVALID_ARG for
  * negative sizes, NULL offsets, or max_seqlen_q = 0 with total_q > 0;
  * FA_ERR_MISALIGNED for offsets not 4-byte aligned.
  */
@@ -342,7 +345,8 @@ fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
  * The work split fa_fwd_prefill would use for a problem on a device with
  * `num_sms` SMs, computed on the host (no device needed).  A unit is one
  * (batch entry, query head, query block of 256 rows for head_dim <= 128, 128
- * for 256); it visits nk = ceil(sk / 128) key blocks.  The grid's first
+ * for 256 and 512); it visits nk = ceil(sk / 128) key blocks; at head_dim 512
+ * it runs as two CTAs and is never split.  The grid's first
  * out[0] CTAs each process a whole unit; the remaining out[1] units (the last
  * partial wave) are each processed by out[2] CTAs, piece i taking key blocks
  * [i nk / out[2], (i + 1) nk / out[2]), and the last piece to finish merges
