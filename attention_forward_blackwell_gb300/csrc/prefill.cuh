@@ -643,8 +643,9 @@ template <class T, bool VARLEN>
 __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                      const CUtensorMap* tm_v, const PrefillArgs& a,
                                      const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
-                                     uint32_t sRing, const WaitCtx& wc) {
+                                     uint32_t sRing, const WaitCtx& wc, unsigned long long* tr) {
     const int lane = threadIdx.x & 31;
+    if (lane != 0) tr = nullptr;
     if (w.n_max <= 0) return;
     const uint32_t bar_q = smem_u32(&aux->bar_q);
     if (lane == 0) {
@@ -664,6 +665,7 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
         if (!mbar_wait(smem_u32(&aux->bar_empty[slot]), ring_phase<T>(p) ^ 1u, wc,
                        kErrWaitTimeout | kSiteLoadEmpty))
             return false;
+        trace_mark(tr, kTrLoad, p >> 4, p & 15);   // position p's copy issued
         const uint32_t full = smem_u32(&aux->bar_full[slot]);
         const uint32_t dst = sRing + slot * T::SLOT;
         const int jk = w.kb + j;
@@ -717,7 +719,7 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
 template <class T>
 __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
                                     PrefillAux<T>* aux, uint32_t tmem, uint32_t sQ,
-                                    uint32_t sRing, const WaitCtx& wc) {
+                                    uint32_t sRing, const WaitCtx& wc, unsigned long long* tr) {
     const int lane = threadIdx.x & 31;
     if (lane != 0) {
         __syncwarp();
@@ -738,9 +740,11 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     };
     auto slot_desc = [&](uint32_t d0) { return d0 + (uint32_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
     // S(buffer sb) = Q K^T, each K piece released once its K-steps complete
-    auto score = [&](int sb) -> bool {
+    // (trace: row j = the block whose scores these are, events 1..8 = pieces)
+    auto score = [&](int sb, int jt) -> bool {
         for (int pc = 0; pc < T::PIECES; ++pc) {
             if (!next_piece(kSiteMmaK)) return false;
+            trace_mark(tr, kTrMma, jt, 1 + pc);
             const uint32_t kd = slot_desc(kd0);
 #pragma unroll
             for (int kin = 0; kin < 4; ++kin) {
@@ -757,7 +761,7 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     if (w.n_max > 0) do {
         if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         tc_fence_after();
-        if (!score(0)) break;
+        if (!score(0, 0)) break;
         bool ok = true;
         for (int j = 0; j < w.n_max && ok; ++j) {
             if (j + 1 < w.n_max) {
@@ -765,17 +769,20 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
                                               sig_par<T>(j - 1), wc, kErrWaitTimeout | kSiteMmaPv))
                     break;
                 tc_fence_after();
-                if (!score((j + 1) & 1)) break;
+                trace_mark(tr, kTrMma, j + 1, 0);   // S(j+1) may start
+                if (!score((j + 1) & 1, j + 1)) break;
             }
             if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                 kErrWaitTimeout | kSiteMmaP))
                 break;
+            trace_mark(tr, kTrMma, j, 9);             // P(j) ready
             tc_fence_after();
             for (int nh = 0; nh < T::VPIECES; ++nh) {
                 if (!next_piece(kSiteMmaV)) {
                     ok = false;
                     break;
                 }
+                trace_mark(tr, kTrMma, j, 10 + nh);   // V piece nh landed
                 issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(j & 1) + 64,
                                slot_desc(vd0), idesc_v, j == 0);
                 tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
@@ -1295,9 +1302,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
         if constexpr (T::DV_SPLIT > 1) {
             if (warp == T::MMA_WARP)
-                prefill_mma_role_dv<T>(args, w, aux, tmem, sQ, sRing, wc);
+                prefill_mma_role_dv<T>(args, w, aux, tmem, sQ, sRing, wc, tr);
             else if (warp == T::LOAD_WARP)
-                prefill_load_role_dv<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc);
+                prefill_load_role_dv<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc,
+                                                tr);
         } else {
             if (warp == T::MMA_WARP)
                 prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);
