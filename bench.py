@@ -47,14 +47,15 @@ KERNEL_SOURCES = {
                "attention_forward_blackwell_gb300/csrc/ptx.cuh",
                "attention_forward_blackwell_gb300/csrc/common.cuh"],
 }
+
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("5bed0a549fc3444a7e7947f8922e79e770a402c95d9b3ea0c079edc80ed110db",
-                120160768, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (463.87 MB) and scaled to batch 64 by the
+    "prefill": ("5f2090474e67d1d39c43c362dfd3b4ef62715398224c0f7bcd97a533a6de2de9",
+                118664448, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
+    # captured at batch 16 (463.45 MB) and scaled to batch 64 by the
     # algorithmic bytes of the two batches
-    "decode": ("ad2a200dae3f194bb625da169552e109cd1851933861a5bd158c043234c1681f",
-               2206446577, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    "decode": ("6c42fe0c85c1b5e1ea69bf2dc9db9e431e10b54b837b8bdfa41a593ca1d3291a",
+               2204452012, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
 }
 
 
