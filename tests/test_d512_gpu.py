@@ -168,3 +168,48 @@ def test_prefill_d512_halves_are_independent_of_each_other():
     assert torch.equal(o2[..., :D // 2], o[..., :D // 2])
     assert torch.all(o2[..., D // 2:] == 0)
     assert torch.equal(lse2, lse)
+
+
+def test_prefill_d512_extreme_logits_one_hot_key():
+    """K*8 and one key whose score is 60 above the rest for every query: the
+    row's weight is all on that key (LSE > 55), and both column halves of O
+    reproduce its value row; the rebase path runs whenever the max jumps."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(1, 2, 2, 300, 300, D, tag=5500, device="cuda", k_scale=8.0)
+    x.q[..., 0] = 4.0
+    x.k[..., 17, :] = 0.0
+    x.k[..., 17, 0] = 60.0 * math.sqrt(D) / 4.0
+    scale = 1.0 / math.sqrt(D)
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale)
+    torch.cuda.synchronize()
+    check_device_error()
+    ro, rl = oracle_for(x, scale, False)
+    compare(o, lse, ro, rl, "d512 extreme logits")
+    assert float(lse.min()) > 55.0
+    assert (o.float() - x.v[:, :, 17:18].float()).abs().max().item() < 2e-2
+
+
+def test_prefill_d512_replays_in_a_cuda_graph():
+    """Captured in a CUDA graph and replayed: every replay equals the eager
+    result bit for bit."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    x = inputs.make_inputs(1, 4, 2, 700, 700, D, tag=5600, device="cuda")
+    o_ref, l_ref = binding.prefill(x.q, x.k, x.v, causal=True)
+    o = torch.empty_like(x.q)
+    lse = torch.empty(1, 4, 700, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up outside the capture
+        binding.prefill(x.q, x.k, x.v, causal=True, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.prefill(x.q, x.k, x.v, causal=True, out=o, lse=lse)
+    for _ in range(3):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    check_device_error()
