@@ -179,7 +179,7 @@ class ClockSampler:
                 sel = []
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 f"-lms", str(self.period_ms)] + sel,
+                 "-lms", str(self.period_ms)] + sel,
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
