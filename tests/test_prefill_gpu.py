@@ -285,3 +285,28 @@ def test_wide_grids(B, Hq, Hkv, S, d, causal):
     idx = torch.from_numpy(rows).cuda()
     compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, f"wide grid {B, Hq, Hkv, S, d}")
     free_cuda()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_context_128k_sampled(causal):
+    """One head over 131,072 keys (up to 1,024 key blocks per unit; the
+    non-causal launch computes the 56 units of its last partial wave in two
+    pieces each, the causal one runs units of 2 to 1,024 blocks heaviest
+    first): finiteness everywhere, sampled rows (tile edges at the start,
+    middle and end plus random rows) against the oracle."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    S, d = 131072, 128
+    if not causal:
+        assert binding.debug_prefill_plan(1, 1, S, S, d, 0, 152) == (456, 56, 2)
+    x = inputs.make_inputs(1, 1, 1, S, S, d, tag=1300, device="cuda")
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    check_device_error()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    rows = sample_rows(1, 1, S, n_random=64, seed=S + causal)
+    ro, rl = oracle_for(x, scale, causal, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, f"128K keys causal={causal}")
+    del x, o, lse
+    free_cuda()
