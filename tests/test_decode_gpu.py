@@ -116,3 +116,25 @@ def test_decode_many_sequences_max_queries_sampled():
     idx = torch.from_numpy(rows).cuda()
     compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, "decode B=256 Sq=16 (sampled)")
     free_cuda()
+
+
+@pytest.mark.parametrize("B,Hq,Sq,lengths,causal", [
+    (2, 8, 1, [1 << 20, 300001], False),   # 1,048,576 keys: ~1,700 splits merged
+    (1, 2, 16, [1 << 20], True),           # the most queries decode takes, causal
+])
+def test_decode_million_keys(B, Hq, Sq, lengths, causal):
+    """A key range of 2^20 (padding past shorter lengths poisoned with NaN):
+    every output row against the oracle."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    d, Sk = 128, 1 << 20
+    x = inputs.make_inputs(B, Hq, 1, Sq, Sk, d, tag=1400 + Sq, device="cuda", lengths=lengths)
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.decode(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k)
+    torch.cuda.synchronize()
+    check_device_error()
+    ro, rl = oracle_for(x, scale, causal)
+    compare(o, lse, ro, rl, f"decode 2^20 keys B={B} Sq={Sq}")
+    del x, o, lse
+    free_cuda()
