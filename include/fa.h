@@ -257,7 +257,13 @@ fa_status fa_fwd_decode_splits(const void *q, const void *k, const void *v,
  *
  * The first call on each device does a one-time set-up with that device
  * current (it resolves the array's device address); make that first call
- * before any stream capture.  All calls on a device share the one array and
+ * before any stream capture.  Under the CUDA runtime's default lazy module
+ * loading, that first call is also what loads this array's module on the
+ * device and so commits its 16 MiB there: make it at start-up, before
+ * another allocator reserves the device's memory (or run with
+ * CUDA_MODULE_LOADING=EAGER, which commits the array when the library's
+ * device code is loaded).  If the array cannot be committed, that call
+ * returns FA_ERR_CUDA.  All calls on a device share the one array and
  * it keeps the last call's contents: nothing in it needs clearing (each call
  * writes every partial it reads), but calls that overlap on the GPU -- on
  * different streams, or from different host threads -- race on it and give

@@ -76,6 +76,41 @@ def test_prefill_paged(B, Hq, Hkv, Sq, Sk, d, P, causal, lengths):
     free_cuda()
 
 
+SPLIT_PAGED = [
+    # B, Hq, Hkv, Sq, Sk, d, page_size, lengths: non-causal shapes with at
+    # least 16 key blocks whose units do not fill a wave, so the plan cuts
+    # them into pieces along the key axis (page lookups inside every piece)
+    (2, 2, 1, 1024, 2560, 128, 256, [2560, 2300]),
+    (1, 4, 2, 512, 2048, 256, 128, [2048]),
+    (2, 2, 2, 1024, 3072, 64, 512, [3000, 2049]),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,P,lengths", SPLIT_PAGED,
+                         ids=[f"b{c[0]}q{c[3]}k{c[4]}d{c[5]}p{c[6]}" for c in SPLIT_PAGED])
+def test_prefill_paged_split_units(B, Hq, Hkv, Sq, Sk, d, P, lengths):
+    """Paged caches with the last wave split into pieces and merged on the
+    device: every row against the oracle, and bit-equal to the same plan on
+    contiguous K/V."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert binding.debug_prefill_plan(B, Hq, Sq, Sk, d, False, n_sms)[2] > 1
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=850 + d, device="cuda", lengths=lengths)
+    kc, vc, table, _ = to_pages(x.k, x.v, lengths, P, seed=P + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill_paged(x.q, kc, vc, table, x.seqlens_k, scale=scale)
+    torch.cuda.synchronize()
+    check_device_error()
+    ro, rl = oracle_for(x, scale, False)
+    compare(o, lse, ro, rl, f"prefill paged split P={P} d={d}")
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    o2, l2 = binding.prefill(x.q, x.k, x.v, scale=scale, seqlens_k=x.seqlens_k)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    free_cuda()
+
+
 DECODE = [
     # B, Hq, Hkv, Sq, Sk, d, page_size
     (8, 8, 2, 1, 4096, 128, 16),
