@@ -107,6 +107,32 @@ bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map {64 columns, rows, d / 64 chunks, planes} (chunk stride 128
+// bytes) with a {64, 128, 2, 1} box: one copy brings two 64-column chunks of
+// a 128-row tile, written to shared memory as [chunk][row][64 columns] with
+// 128-byte swizzle, the same bytes as two boxes of the 3-D map.  d must be a
+// multiple of 128.
+bool encode_map4_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
+                         unsigned long long row_stride, unsigned long long plane_stride) {
+    const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64), (cuuint64_t)planes};
+    const cuuint64_t strides[3] = {(cuuint64_t)row_stride, 128, (cuuint64_t)plane_stride};
+    const cuuint32_t box[4] = {64, 128, 2, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Load maps of the prefill kernels: 4-D (two chunks per copy) for head_dim
+// 128 and 256, 3-D otherwise.
+bool prefill_load_map(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
+                      unsigned long long row_stride, unsigned long long plane_stride) {
+    if (d == 128 || d == 256)
+        return encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride);
+    return encode_map_strided(m, base, d, rows, planes, row_stride, plane_stride);
+}
+
 bool encode_map(CUtensorMap* m, const void* base, int d, int rows, long long planes) {
     return encode_map_strided(m, base, d, rows, planes, (unsigned long long)d * 2,
                               (unsigned long long)rows * d * 2);
@@ -267,24 +293,31 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     // Q, O: token-major packed tensors (map {d, tokens, heads}, a token's
     // heads adjacent) or dense [B, Hq, Sq, d]; K, V: paged caches, packed or
     // dense
+    // (loads: prefill_load_map; the O store map is 3-D)
     if (vl) {
-        if (!encode_map_strided(&p.tm_q, q, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes) ||
+        if (!prefill_load_map(&p.tm_q, q, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes) ||
             !encode_map_strided(&p.tm_o, o, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes))
             return FA_ERR_INVALID_ARG;
-    } else if (!encode_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq) ||
+    } else if (!prefill_load_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq, row_bytes,
+                                 row_bytes * sq) ||
                !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq)) {
         return FA_ERR_INVALID_ARG;
     }
     if (block_table) {
-        if (!encode_map(&p.tm_k, k, head_dim, page_size, (long long)num_pages * hkv) ||
-            !encode_map(&p.tm_v, v, head_dim, page_size, (long long)num_pages * hkv))
+        const long long planes = (long long)num_pages * hkv;
+        if (!prefill_load_map(&p.tm_k, k, head_dim, page_size, planes, row_bytes,
+                              row_bytes * page_size) ||
+            !prefill_load_map(&p.tm_v, v, head_dim, page_size, planes, row_bytes,
+                              row_bytes * page_size))
             return FA_ERR_INVALID_ARG;
     } else if (vl) {
-        if (!encode_map_strided(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
-            !encode_map_strided(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes))
+        if (!prefill_load_map(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
+            !prefill_load_map(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes))
             return FA_ERR_INVALID_ARG;
-    } else if (!encode_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv) ||
-               !encode_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv)) {
+    } else if (!prefill_load_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv, row_bytes,
+                                 row_bytes * sk) ||
+               !prefill_load_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv, row_bytes,
+                                 row_bytes * sk)) {
         return FA_ERR_INVALID_ARG;
     }
     PrefillArgs& a = p.args;

@@ -57,6 +57,16 @@
 namespace fa {
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units (a factor of 256)
+
+#ifndef FA_MMA_SPIN
+#define FA_MMA_SPIN 0
+#endif
+#ifndef FA_SM_SPIN
+#define FA_SM_SPIN 0
+#endif
+constexpr bool kMmaSpin = FA_MMA_SPIN != 0;   // MMA lane polls its barriers without suspending
+constexpr bool kSmSpin = FA_SM_SPIN != 0;     // softmax warps poll "S ready" without suspending
+
 // Optionally (kUsePolyExp2), in tiles without masked entries one pair of
 // exponentials in every kPolyEvery is computed by exp2_poly_x2 on the FMA
 // pipe instead of the MUFU ex2 instruction.  Measured on GB300 this is slower
@@ -81,6 +91,20 @@ struct PrefillTraits {
     // O), because 512 fp32 O columns leave no tensor memory for the scores.
     static constexpr int DV_SPLIT = (D == 512) ? 2 : 1;
     static constexpr int D_COLS = D / DV_SPLIT;        // O accumulator columns of a CTA
+    // One Q tile (head_dim >= 256): the ring is filled in the order the MMA
+    // warp consumes it (K_0, then K_{j+1} before V_j) and each slot is
+    // released as soon as the MMAs that read it complete.
+    static constexpr bool CONSUME_ORDER = (D >= 256);
+    // head_dim 128 and 256: the Q, K and V tensor maps are 4-D, {64 columns,
+    // rows, 64-column chunks, planes} with a chunk stride of 128 bytes, and
+    // one copy brings a {64, 128, 2, 1} box: two chunks (32 KB) written as
+    // [chunk][row][64 columns], the layout of two 3-D boxes.  The SM's copy
+    // engine spends about as long on a box of 2 x 128 rows as on one of 128
+    // rows (measured on GB300: ~350 vs ~235 cycles at full occupancy), so
+    // this cuts its time per key block by a quarter.  (head_dim 96 keeps 3-D
+    // boxes: its second chunk is half a row, and a 4-D box would read the
+    // next row's first columns into it, past the tensor at its last row.)
+    static constexpr bool BOX4 = (D == 128 || D == 256);
     static constexpr int OCH = (D_COLS + 63) / 64;     // 64-column chunks of a CTA's O
     // chunks per ring slot: one at head_dim 512 (the 128 KB Q tile leaves
     // room for five 16 KB slots only)
@@ -316,6 +340,23 @@ __device__ __forceinline__ uint32_t ring_slot(int p) { return (uint32_t)(p % T::
 template <class T>
 __device__ __forceinline__ uint32_t ring_phase(int p) { return (uint32_t)((p / T::NSLOT) & 1); }
 
+// Loads N consecutive 64-column chunks, starting at chunk c0, of the
+// 128-row tile at (row, plane) into consecutive CHUNK-byte buffers at dst
+// (4-D maps: two chunks per copy; 3-D maps: one).  Issued by one lane.
+template <class T, int N>
+__device__ __forceinline__ void load_chunks(uint32_t dst, const CUtensorMap* m, int c0, int row,
+                                            int plane, uint32_t bar) {
+    if constexpr (T::BOX4) {
+        static_assert(N % 2 == 0, "4-D boxes carry two chunks");
+#pragma unroll
+        for (int c = 0; c < N; c += 2)
+            tma_load_4d(dst + c * T::CHUNK, m, 0, row, c0 + c, plane, bar);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N; ++c) tma_load_3d(dst + c * T::CHUNK, m, (c0 + c) * 64, row, plane, bar);
+    }
+}
+
 // Zeroes rows [rv, BN) of every 64-column chunk of one ring slot (all 32
 // lanes of the calling warp), then makes the writes visible to the tensor
 // core (async proxy).
@@ -352,12 +393,21 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         mbar_arrive_expect_tx(bar_q, (uint32_t)(T::NQ * T::QTILE));
 #pragma unroll
         for (int t = 0; t < T::NQ; ++t)
-#pragma unroll
-            for (int c = 0; c < T::NCH; ++c)
-                tma_load_3d(sQ + t * T::QTILE + c * T::CHUNK, tm_q, c * 64,
-                            (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
-                            VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
+            load_chunks<T, T::NCH>(sQ + t * T::QTILE, tm_q, 0,
+                                   (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
+                                   VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
     }
+    // tile coordinates of key block jk: contiguous K/V, or a page of the
+    // paged caches (packed sequences: token k0 + row of head hk)
+    auto coords = [&](int jk, int& ty, int& tz) {
+        ty = (VARLEN ? w.k0 : 0) + jk * T::BN;
+        tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
+        if (a.block_table != nullptr) {
+            const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
+            ty = ty % a.page_size;
+            tz = page * a.Hkv + w.hk;   // out-of-range pages read as zeros (TMA bounds)
+        }
+    };
     int issued = 0;
     const int total = 2 * w.n_max * T::PIECES;
     for (int p = 0; p < total; ++p) {
@@ -372,14 +422,8 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         const uint32_t full = smem_u32(&aux->bar_full[slot]);
         const int jk = w.kb + j;          // key block
         const int rv = w.L - jk * T::BN;  // valid rows of this tile
-        // tile coordinates: contiguous K/V, or a page of the paged caches
-        // (packed sequences: token k0 + j of head hk)
-        int ty = (VARLEN ? w.k0 : 0) + jk * T::BN, tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
-        if (a.block_table != nullptr) {
-            const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
-            ty = ty % a.page_size;
-            tz = page * a.Hkv + w.hk;   // out-of-range pages read as zeros (TMA bounds)
-        }
+        int ty, tz;
+        coords(jk, ty, tz);
         if (kv == 1 && j == w.n_max - 1 && rv < T::BN) {
             // Partial last value tile: rows [rv, BN) may hold anything (and a
             // zero probability times a non-finite value would poison O), so
@@ -387,21 +431,16 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
             const uint32_t tail = smem_u32(&aux->bar_tail);
             if (lane == 0) {
                 mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
-#pragma unroll
-                for (int c = 0; c < T::SLOT_CH; ++c)
-                    tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, tm_v,
-                                (pc * T::SLOT_CH + c) * 64, ty, tz, tail);
+                load_chunks<T, T::SLOT_CH>(sRing + slot * T::SLOT, tm_v, pc * T::SLOT_CH, ty, tz,
+                                           tail);
             }
             if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail)) break;
             zero_value_tail<T>(sRing + slot * T::SLOT, rv);
             if (lane == 0) mbar_arrive(full);
         } else if (lane == 0) {
             mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
-            const CUtensorMap* m = kv ? tm_v : tm_k;
-#pragma unroll
-            for (int c = 0; c < T::SLOT_CH; ++c)
-                tma_load_3d(sRing + slot * T::SLOT + c * T::CHUNK, m, (pc * T::SLOT_CH + c) * 64,
-                            ty, tz, full);
+            load_chunks<T, T::SLOT_CH>(sRing + slot * T::SLOT, kv ? tm_v : tm_k, pc * T::SLOT_CH,
+                                       ty, tz, full);
         }
         __syncwarp();
         issued = p + 1;
@@ -475,7 +514,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     auto empty_bar = [&](int p) { return smem_u32(&aux->bar_empty[ring_slot<T>(p)]); };
     auto wait_tile = [&](int p0, unsigned site) {
         for (int pc = 0; pc < T::PIECES; ++pc)
-            if (!mbar_wait_lane(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
+            if (!mbar_wait_lane<kMmaSpin>(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
                 return false;
         return true;
     };
@@ -500,7 +539,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     uint32_t kd[T::PIECES];
 
     if (w.n_max > 0) do {
-        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         if constexpr (T::NQ == 2) {
             // one issuing warp alternates the tiles: PV_0(j), S_0(j+1),
             // PV_1(j), S_1(j+1); each softmax overlaps the other tile's MMAs
@@ -527,7 +566,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j >= w.n_kv[t]) continue;
-                    if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]),
+                    if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]),
                                         sig_par<T>(j), wc,
                                    kErrWaitTimeout | kSiteMmaP)) {
                         ok = false;
@@ -553,7 +592,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                             kdesc(posK, kd);
                         }
                         // S_t(j+1) overwrites P_t(j): PV_t(j) must have completed
-                        if (!mbar_wait_lane(smem_u32(&aux->bar_pv_done[t]), ph, wc,
+                        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[t]), ph, wc,
                                        kErrWaitTimeout | kSiteMmaPv)) {
                             ok = false;
                             break;
@@ -586,7 +625,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 // P(j-1), so PV(j-1) must have completed
                 if (j + 1 < w.n_max) {
                     if (!wait_tile(posK, kSiteMmaK)) break;
-                    if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                    if (j >= 1 && !mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
                                                   sig_par<T>(j - 1), wc,
                                                   kErrWaitTimeout | kSiteMmaPv))
                         break;
@@ -600,7 +639,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 }
                 if (!wait_tile(posV, kSiteMmaV)) break;
                 trace_mark(tr, kTrMma, j, 0);
-                if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
+                if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                kErrWaitTimeout | kSiteMmaP))
                     break;
                 trace_mark(tr, kTrMma, j, 1);
@@ -653,10 +692,8 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
         tma_prefetch_desc(tm_k);
         tma_prefetch_desc(tm_v);
         mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
-#pragma unroll
-        for (int c = 0; c < T::NCH; ++c)
-            tma_load_3d(sQ + c * T::CHUNK, tm_q, c * 64, (VARLEN ? w.q0 : 0) + w.row0,
-                        VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
+        load_chunks<T, T::NCH>(sQ, tm_q, 0, (VARLEN ? w.q0 : 0) + w.row0,
+                               VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
     }
     int p = 0;   // ring position of the next piece
     // one 64-column chunk of K_j (is_v = false) or of this CTA's part of V_j
@@ -676,13 +713,13 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
             ty = ty % a.page_size;
             tz = page * a.Hkv + w.hk;
         }
-        const int x = pc * 64 + (is_v ? w.dv0 : 0);
+        const int c0 = pc * T::SLOT_CH + (is_v ? w.dv0 / 64 : 0);   // first chunk of the slot
         if (is_v && j == w.n_max - 1 && rv < T::BN) {
             // partial last value tile: rows [rv, BN) zeroed before publication
             const uint32_t tail = smem_u32(&aux->bar_tail);
             if (lane == 0) {
                 mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
-                tma_load_3d(dst, tm_v, x, ty, tz, tail);
+                load_chunks<T, T::SLOT_CH>(dst, tm_v, c0, ty, tz, tail);
             }
             if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail))
                 return false;
@@ -690,7 +727,7 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
             if (lane == 0) mbar_arrive(full);
         } else if (lane == 0) {
             mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
-            tma_load_3d(dst, is_v ? tm_v : tm_k, x, ty, tz, full);
+            load_chunks<T, T::SLOT_CH>(dst, is_v ? tm_v : tm_k, c0, ty, tz, full);
         }
         __syncwarp();
         ++p;
@@ -732,7 +769,7 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
     int p = 0;   // ring position of the next piece (the producer's order)
     auto next_piece = [&](unsigned site) -> bool {
-        if (!mbar_wait_lane(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
+        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
                             kErrWaitTimeout | site))
             return false;
         tc_fence_after();
@@ -747,8 +784,8 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
             trace_mark(tr, kTrMma, jt, 1 + pc);
             const uint32_t kd = slot_desc(kd0);
 #pragma unroll
-            for (int kin = 0; kin < 4; ++kin) {
-                const int kk = pc * 4 + kin;
+            for (int kin = 0; kin < T::SLOT_CH * 4; ++kin) {
+                const int kk = pc * T::SLOT_CH * 4 + kin;
                 umma_ss_lo(tmem + T::s_col(sb), qd0 + kstep_off(kk), kd + kstep_off(kin), idesc_s,
                            kk > 0 ? 1u : 0u);
             }
@@ -759,20 +796,20 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
         return true;
     };
     if (w.n_max > 0) do {
-        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         tc_fence_after();
         if (!score(0, 0)) break;
         bool ok = true;
         for (int j = 0; j < w.n_max && ok; ++j) {
             if (j + 1 < w.n_max) {
-                if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                if (j >= 1 && !mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
                                               sig_par<T>(j - 1), wc, kErrWaitTimeout | kSiteMmaPv))
                     break;
                 tc_fence_after();
                 trace_mark(tr, kTrMma, j + 1, 0);   // S(j+1) may start
                 if (!score((j + 1) & 1, j + 1)) break;
             }
-            if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
+            if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                 kErrWaitTimeout | kSiteMmaP))
                 break;
             trace_mark(tr, kTrMma, j, 9);             // P(j) ready
@@ -829,7 +866,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         {
             const uint32_t bar_s = smem_u32(&aux->bar_s_full[(T::NQ == 2) ? t : sb]);
             const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
-            if (!mbar_wait(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
+            if (!mbar_wait<kSmSpin>(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
                 ok = false;
                 break;
             }
@@ -1300,7 +1337,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             &tm_o, args, w, aux, tmem, sQ, wc, tr);
     } else {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
-        if constexpr (T::DV_SPLIT > 1) {
+        if constexpr (T::CONSUME_ORDER) {
             if (warp == T::MMA_WARP)
                 prefill_mma_role_dv<T>(args, w, aux, tmem, sQ, sRing, wc, tr);
             else if (warp == T::LOAD_WARP)
