@@ -90,9 +90,8 @@ unsigned long long next_prefill_epoch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D bf16 tensor map over [planes][rows][d] with a {64, 128, 1} box and
-// 128-byte swizzle (rows past `rows` and columns past `d` read as zero).
-// 3-D bf16 map {d, rows, planes} with a 64 x 128 x 1 box and 128-byte swizzle.
+// 3-D bf16 map {d, rows, planes} with a {64, 128, 1} box and 128-byte
+// swizzle (rows past `rows` and columns past `d` read as zero).
 // Strides in bytes: row_stride between rows, plane_stride between planes
 // (contiguous [planes][rows][d] when they are d * 2 and rows * d * 2).
 bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
@@ -125,10 +124,10 @@ bool encode_map4_strided(CUtensorMap* m, const void* base, int d, long long rows
 }
 
 // Load maps of the prefill kernels: 4-D (two chunks per copy) for head_dim
-// 128 and 256, 3-D otherwise.
+// 256, 3-D otherwise.
 bool prefill_load_map(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
                       unsigned long long row_stride, unsigned long long plane_stride) {
-    if (d == 128 || d == 256)
+    if (d == 256)
         return encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride);
     return encode_map_strided(m, base, d, rows, planes, row_stride, plane_stride);
 }

@@ -58,14 +58,6 @@ namespace fa {
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units (a factor of 256)
 
-#ifndef FA_MMA_SPIN
-#define FA_MMA_SPIN 0
-#endif
-#ifndef FA_SM_SPIN
-#define FA_SM_SPIN 0
-#endif
-constexpr bool kMmaSpin = FA_MMA_SPIN != 0;   // MMA lane polls its barriers without suspending
-constexpr bool kSmSpin = FA_SM_SPIN != 0;     // softmax warps poll "S ready" without suspending
 
 // Optionally (kUsePolyExp2), in tiles without masked entries one pair of
 // exponentials in every kPolyEvery is computed by exp2_poly_x2 on the FMA
@@ -95,16 +87,17 @@ struct PrefillTraits {
     // warp consumes it (K_0, then K_{j+1} before V_j) and each slot is
     // released as soon as the MMAs that read it complete.
     static constexpr bool CONSUME_ORDER = (D >= 256);
-    // head_dim 128 and 256: the Q, K and V tensor maps are 4-D, {64 columns,
-    // rows, 64-column chunks, planes} with a chunk stride of 128 bytes, and
-    // one copy brings a {64, 128, 2, 1} box: two chunks (32 KB) written as
+    // head_dim 256: the Q, K and V tensor maps are 4-D, {64 columns, rows,
+    // 64-column chunks, planes} with a chunk stride of 128 bytes, and one
+    // copy brings a {64, 128, 2, 1} box: two chunks (32 KB) written as
     // [chunk][row][64 columns], the layout of two 3-D boxes.  The SM's copy
     // engine spends about as long on a box of 2 x 128 rows as on one of 128
-    // rows (measured on GB300: ~350 vs ~235 cycles at full occupancy), so
-    // this cuts its time per key block by a quarter.  (head_dim 96 keeps 3-D
-    // boxes: its second chunk is half a row, and a 4-D box would read the
-    // next row's first columns into it, past the tensor at its last row.)
-    static constexpr bool BOX4 = (D == 128 || D == 256);
+    // rows (measured on GB300: ~350 vs ~235 cycles at full occupancy), which
+    // matters where a key block brings 128 KB.  (At head_dim 128 the same
+    // boxes measured 1 % slower; head_dim 96 cannot use them: its second
+    // chunk is half a row, and a 4-D box would read the next row's first
+    // columns into it, past the tensor at its last row.)
+    static constexpr bool BOX4 = (D == 256);
     static constexpr int OCH = (D_COLS + 63) / 64;     // 64-column chunks of a CTA's O
     // chunks per ring slot: one at head_dim 512 (the 128 KB Q tile leaves
     // room for five 16 KB slots only)
@@ -514,7 +507,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     auto empty_bar = [&](int p) { return smem_u32(&aux->bar_empty[ring_slot<T>(p)]); };
     auto wait_tile = [&](int p0, unsigned site) {
         for (int pc = 0; pc < T::PIECES; ++pc)
-            if (!mbar_wait_lane<kMmaSpin>(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
+            if (!mbar_wait_lane(full_bar(p0 + pc), ring_phase<T>(p0 + pc), wc, kErrWaitTimeout | site))
                 return false;
         return true;
     };
@@ -539,7 +532,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
     uint32_t kd[T::PIECES];
 
     if (w.n_max > 0) do {
-        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         if constexpr (T::NQ == 2) {
             // one issuing warp alternates the tiles: PV_0(j), S_0(j+1),
             // PV_1(j), S_1(j+1); each softmax overlaps the other tile's MMAs
@@ -566,7 +559,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
                     if (j >= w.n_kv[t]) continue;
-                    if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]),
+                    if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]),
                                         sig_par<T>(j), wc,
                                    kErrWaitTimeout | kSiteMmaP)) {
                         ok = false;
@@ -592,7 +585,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                             kdesc(posK, kd);
                         }
                         // S_t(j+1) overwrites P_t(j): PV_t(j) must have completed
-                        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[t]), ph, wc,
+                        if (!mbar_wait_lane(smem_u32(&aux->bar_pv_done[t]), ph, wc,
                                        kErrWaitTimeout | kSiteMmaPv)) {
                             ok = false;
                             break;
@@ -625,7 +618,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 // P(j-1), so PV(j-1) must have completed
                 if (j + 1 < w.n_max) {
                     if (!wait_tile(posK, kSiteMmaK)) break;
-                    if (j >= 1 && !mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                    if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
                                                   sig_par<T>(j - 1), wc,
                                                   kErrWaitTimeout | kSiteMmaPv))
                         break;
@@ -639,7 +632,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                 }
                 if (!wait_tile(posV, kSiteMmaV)) break;
                 trace_mark(tr, kTrMma, j, 0);
-                if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
+                if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                kErrWaitTimeout | kSiteMmaP))
                     break;
                 trace_mark(tr, kTrMma, j, 1);
@@ -769,7 +762,7 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
     int p = 0;   // ring position of the next piece (the producer's order)
     auto next_piece = [&](unsigned site) -> bool {
-        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
+        if (!mbar_wait_lane(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
                             kErrWaitTimeout | site))
             return false;
         tc_fence_after();
@@ -796,20 +789,20 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
         return true;
     };
     if (w.n_max > 0) do {
-        if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
+        if (!mbar_wait_lane(smem_u32(&aux->bar_q), 0, wc, kErrWaitTimeout | kSiteMmaQ)) break;
         tc_fence_after();
         if (!score(0, 0)) break;
         bool ok = true;
         for (int j = 0; j < w.n_max && ok; ++j) {
             if (j + 1 < w.n_max) {
-                if (j >= 1 && !mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
+                if (j >= 1 && !mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, j - 1)]),
                                               sig_par<T>(j - 1), wc, kErrWaitTimeout | kSiteMmaPv))
                     break;
                 tc_fence_after();
                 trace_mark(tr, kTrMma, j + 1, 0);   // S(j+1) may start
                 if (!score((j + 1) & 1, j + 1)) break;
             }
-            if (!mbar_wait_lane<kMmaSpin>(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
+            if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, j)]), sig_par<T>(j), wc,
                                 kErrWaitTimeout | kSiteMmaP))
                 break;
             trace_mark(tr, kTrMma, j, 9);             // P(j) ready
@@ -866,7 +859,7 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         {
             const uint32_t bar_s = smem_u32(&aux->bar_s_full[(T::NQ == 2) ? t : sb]);
             const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
-            if (!mbar_wait<kSmSpin>(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
+            if (!mbar_wait(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
                 ok = false;
                 break;
             }

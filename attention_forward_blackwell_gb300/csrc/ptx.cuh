@@ -88,19 +88,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking test of the phase with the given parity.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // Shared state of the bounded waits of one CTA: a time limit, a CTA-wide
 // abort flag in shared memory and the device error word in global memory.
 // Kept small (four registers) because every wait site is inlined.
@@ -122,16 +109,12 @@ __device__ __forceinline__ void record_error(const WaitCtx& w, unsigned int code
 // One lane's bounded wait for the phase of `bar` with the given parity.
 // Returns false (without having observed the phase) if the CTA was aborted or
 // the wait exceeded the time limit; the latter records `code`.
-// SPIN: poll with the non-blocking test instead of the potentially
-// suspending try_wait (for waits on the critical path of a pipeline).
-template <bool SPIN = false>
 __device__ __forceinline__ bool mbar_wait_lane(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                                unsigned int code) {
-    auto poll = [&]() { return SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity); };
-    if (poll()) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     const uint32_t t0 = globaltimer_lo();
     for (uint32_t it = 1;; ++it) {
-        if (poll()) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0u) {
             if (ld_volatile_shared(w.abort_flag)) return false;
             if (globaltimer_lo() - t0 > w.limit_ns) {
@@ -144,10 +127,9 @@ __device__ __forceinline__ bool mbar_wait_lane(uint32_t bar, uint32_t parity, co
 
 // Bounded wait executed by all 32 lanes of a warp; the result is uniform
 // across the warp, so warp-collective instructions after it never diverge.
-template <bool SPIN = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w,
                                           unsigned int code) {
-    const bool ok = mbar_wait_lane<SPIN>(bar, parity, w, code);
+    const bool ok = mbar_wait_lane(bar, parity, w, code);
     return __all_sync(0xffffffffu, ok);
 }
 

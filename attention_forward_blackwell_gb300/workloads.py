@@ -71,6 +71,9 @@ LONG_D128 = Workload("long_prefill_b1_h16_s8192_d128", 1, 16, 16, 8192, 8192,
 LONG_D96 = Workload("prefill_b2_h16_s4096_d96", 2, 16, 16, 4096, 4096, 96,
                     False, 6,
                     description="prefill MHA B=2 H=16 Sq=Sk=4096 d=96 non-causal")
+# head_dim 64 at the shape of the last row of the "fa4-sm120-research" table
+PREFILL_D64 = Workload("prefill_b4_h32_s2048_d64", 4, 32, 32, 2048, 2048, 64, False, 8,
+                       description="prefill MHA B=4 H=32 Sq=Sk=2048 d=64 non-causal")
 GQA_D256 = Workload("causal_gqa_b4_hq32_hkv4_s2048_d256", 4, 32, 4, 2048, 2048,
                     256, True, 4, k_scale=0.5,
                     description="causal GQA B=4 Hq=32 Hkv=4 Sq=Sk=2048 d=256, K*0.5")
@@ -87,5 +90,5 @@ DECODE = Workload("decode_gqa_b64_hq64_hkv8_d128", 64, 64, 8, 1, 16384, 128,
                   description="decode GQA B=64 Hq=64 Hkv=8 Sq=1 d=128, "
                               "L_b~U[1024,16384], KV padded to 16384")
 
-ALL = [TINY, PREFILL_D128, PREFILL_D128_CAUSAL, LONG_D128, LONG_D96, GQA_D256,
+ALL = [TINY, PREFILL_D128, PREFILL_D128_CAUSAL, LONG_D128, LONG_D96, PREFILL_D64, GQA_D256,
        PREFILL_D512, PREFILL_D512_CAUSAL, DECODE]

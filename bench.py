@@ -1,20 +1,28 @@
 """Benchmark of the attention forward hot path on GB300.
 
-One step = the prefill workload "B=2, H=16, Sq=Sk=4096, d=128", run once
-non-causal and once causal (two launches of the tcgen05 prefill kernel),
-with inputs resident in HBM and L2 flushed between steps.  The JSON line's
-``value`` is whole-job TFLOPS (4*B*H*S^2*d per non-causal pass, half for the
-causal pass).  The same run also times the decode workload (B=64, Hq=64,
-Hkv=8, d=128, key lengths ~U[1024, 16384] padded to 16384) in GB/s, and the
-end-to-end path through the C ABI with host buffers (inputs copied in,
-outputs copied back inside the timed region).
+One step runs every configuration of the hot path once per repetition: the
+long prefill "B=1, H=16, Sq=Sk=8192, d=128" (the headline: the largest
+prefill configuration, and the shape of the "fa4-sm120-research" throughput
+table's first row), the prefill "B=2, H=16, S=4096, d=128" non-causal and
+causal, its d=96 variant, the causal GQA "B=4, Hq=32, Hkv=4, S=2048, d=256"
+(K scaled by 0.5), head_dim 64 at "B=4, H=32, S=2048" (the table's last
+row), the tiny "B=1, H=1, S=128, d=64" (latency, in us) and the split-KV
+decode "B=64, Hq=64, Hkv=8, d=128" with key lengths ~U[1024, 16384] (GB/s).
+Every launch is timed on its own with CUDA events after an L2 flush
+(a 512 MiB write outside the events); each configuration gets at least 50
+timed launches (repetitions per step = ceil(50 / steps)) and reports the
+median.  ``value`` is the headline configuration's TFLOPS (4*B*H*S^2*d over
+its median time).  ``e2e`` is the headline configuration through the C ABI
+fed from pinned host buffers (inputs copied in and outputs copied back inside
+the timed region).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 ``--impl reference`` times the fp64 CPU oracle (the test suite's reference
-implementation) on a bounded sample of the same workload, on the host cores.
-With N > 1 (launched by torchrun) every rank runs the same per-GPU workload
-(weak scaling, no collective in the data path); times are the max over ranks.
+implementation) on a bounded sample of the headline configuration, on the
+host cores.  With N > 1 (launched by torchrun) each configuration's
+(batch entry, key/value head) pairs are dealt out over the ranks (shard_plan;
+no collective in the data path) and times are the max over ranks.
 """
 from __future__ import annotations
 
@@ -33,12 +41,16 @@ if ROOT not in sys.path:
 
 METRIC = "prefill fwd TFLOPS & % bf16 tensor peak; decode HBM GB/s & % peak (1×GB300)"
 FLUSH_BYTES = 512 << 20
+MIN_REPS = 50
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The pages' own forward figure for the headline shape (b=1, s=8192, h=16,
+# d=128), measured on an RTX PRO 6000 (SM120): context, not a target.
+PAGES_FWD_TFLOPS_B1_S8192_H16_D128 = 275.5
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
-# the ncu captures summarised under profiles/, keyed by the sha256 of the
-# kernel sources at capture time.  A source change makes the entry stale, and
-# stale entries are reported as null.
+# one ncu capture of the named kernel, keyed by the sha256 of the kernel
+# sources at capture time.  A source change makes the entry stale, and stale
+# entries are reported as null.
 KERNEL_SOURCES = {
     "prefill": ["attention_forward_blackwell_gb300/csrc/prefill.cuh",
                 "attention_forward_blackwell_gb300/csrc/ptx.cuh",
@@ -49,13 +61,13 @@ KERNEL_SOURCES = {
 }
 
 CAPTURED_TRAFFIC = {
-    # kernel: (sources sha256, bytes per launch, profile summary)
-    "prefill": ("5f2090474e67d1d39c43c362dfd3b4ef62715398224c0f7bcd97a533a6de2de9",
-                118664448, "profiles/prefill_kernel_d128_noncausal_b2_h16_s4096.md"),
-    # captured at batch 16 (463.45 MB) and scaled to batch 64 by the
-    # algorithmic bytes of the two batches
-    "decode": ("6c42fe0c85c1b5e1ea69bf2dc9db9e431e10b54b837b8bdfa41a593ca1d3291a",
-               2204452012, "profiles/decode_split_kernel_b16_hq64_hkv8_d128.md"),
+    # kernel: (sources sha256, workload, bytes per launch)
+    "prefill": ("6ba2a761abb15ac241ac2efe7f64487ac98d5e2d2f44628128000fdc935f584b",
+                "long_prefill_b1_h16_s8192_d128", 120440320),
+    # captured at batch 16 (463.38 MB, 1.016 x its algorithmic bytes) and
+    # scaled to batch 64 by the algorithmic bytes of the two batches
+    "decode": ("79e7d7158f673c9efdb21fe2730b9739c7ce55f296f7439f1974e90901f86ec3",
+               "decode_gqa_b64_hq64_hkv8_d128", 2204106190),
 }
 
 
@@ -68,29 +80,28 @@ def sources_hash(kernel):
     return h.hexdigest()
 
 
-def captured_traffic(kernel):
+def captured_traffic(kernel, workload):
     entry = CAPTURED_TRAFFIC.get(kernel)
-    if entry is None or entry[0] != sources_hash(kernel):
+    if entry is None or entry[0] != sources_hash(kernel) or entry[1] != workload:
         return None
-    return entry[1]
+    return entry[2]
 
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=400)
-    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-e2e", action="store_true")
-    p.add_argument("--no-decode", action="store_true")
     p.add_argument("--decode-batch", type=int, default=None,
-                   help="batch of the decode leg (default: the workload's 64); a "
+                   help="batch of the decode configuration (default: the workload's 64); a "
                         "smaller batch keeps profiler captures small")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="budget of the CPU (oracle) baseline sample")
     p.add_argument("--only", default=None, metavar="WORKLOAD",
-                   help="time one named prefill workload alone (e.g. for a profiler "
-                        "capture of its kernel) and print its median; not the bench line")
+                   help="time one named workload alone (e.g. for a profiler capture of its "
+                        "kernel) and print its median; not the bench line")
     return p.parse_args(argv)
 
 
@@ -153,6 +164,33 @@ def reduce_max(pg, value: float) -> float:
 def aggregate(per_rank_units: float, world: int, max_seconds: float) -> float:
     """Whole-job throughput: units processed by all ranks / slowest rank's time."""
     return per_rank_units * world / max_seconds
+
+
+def shard_plan(B: int, Hkv: int, world: int, rank: int):
+    """This rank's share of one problem's (batch entry, key/value head) pairs.
+
+    The B * Hkv pairs, in (batch entry, kv head) order, are dealt out in
+    contiguous ranges of equal size (within one pair); a rank's range is
+    returned as rectangles (b0, b1, hk0, hk1) that are each one contiguous
+    slice of the [B, H, S, d] tensors: whole batch entries, or a range of kv
+    heads (with their query heads) of one batch entry.  Every pair belongs to
+    exactly one rank, so the ranks together compute the whole problem once
+    and exchange nothing.
+    """
+    n = B * Hkv
+    p, p1 = n * rank // world, n * (rank + 1) // world
+    segs = []
+    while p < p1:
+        b, hk = divmod(p, Hkv)
+        if hk == 0 and p1 - p >= Hkv:
+            nb = (p1 - p) // Hkv
+            segs.append((b, b + nb, 0, Hkv))
+            p += nb * Hkv
+        else:
+            e = min(p1, (b + 1) * Hkv)
+            segs.append((b, b + 1, hk, e - b * Hkv))
+            p = e
+    return segs
 
 
 # ----------------------------------------------------------------- clocks ----
@@ -220,155 +258,231 @@ class ClockSampler:
 
 # --------------------------------------------------------------- our arm ----
 
-def _events(torch, n):
-    return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(n)]
+def bench_workloads(decode_batch=None):
+    """(key, workload) pairs of one step, the headline first."""
+    from attention_forward_blackwell_gb300 import workloads as W
+    dec = W.DECODE
+    if decode_batch is not None and decode_batch != dec.B:
+        import dataclasses
+        dec = dataclasses.replace(dec, B=int(decode_batch), name=f"{dec.name}_batch{decode_batch}")
+    return [("long_d128", W.LONG_D128), ("d128", W.PREFILL_D128),
+            ("d128_causal", W.PREFILL_D128_CAUSAL), ("d96", W.LONG_D96),
+            ("gqa_d256_causal", W.GQA_D256), ("d64", W.PREFILL_D64), ("tiny_d64", W.TINY),
+            ("decode", dec)]
+
+
+class Case:
+    """One workload's resident inputs and outputs on this rank, and the
+    launches of this rank's shard of it (one per shard_plan rectangle)."""
+
+    def __init__(self, w, dev, world, rank):
+        import torch
+        from attention_forward_blackwell_gb300 import inputs
+        self.w = w
+        self.x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device=dev,
+                                    k_scale=w.k_scale, lengths=w.lengths)
+        self.o = torch.empty_like(self.x.q)
+        self.lse = torch.empty(w.B, w.Hq, w.Sq, device=dev)
+        self.segs = shard_plan(w.B, w.Hkv, world, rank)
+        G = w.Hq // w.Hkv
+        self.views = []
+        for b0, b1, k0, k1 in self.segs:
+            sl = None if self.x.seqlens_k is None else self.x.seqlens_k[b0:b1]
+            self.views.append((self.x.q[b0:b1, k0 * G:k1 * G], self.x.k[b0:b1, k0:k1],
+                               self.x.v[b0:b1, k0:k1], sl, self.o[b0:b1, k0 * G:k1 * G],
+                               self.lse[b0:b1, k0 * G:k1 * G]))
+        if w.decode:
+            lens = self.x.seqlens_k.cpu().tolist()
+            self.units = W_decode_bytes(w, lens)          # algorithmic bytes
+            self.launches = 2 * len(self.segs)            # split + combine kernels
+        else:
+            self.units = W_prefill_flops(w)
+            self.launches = len(self.segs)
+
+    def run(self, stream=None):
+        from attention_forward_blackwell_gb300 import binding
+        w = self.w
+        for q, k, v, sl, o, lse in self.views:
+            if w.decode:
+                binding.decode(q, k, v, scale=w.scale, causal=w.causal, seqlens_k=sl, out=o,
+                               lse=lse, stream=stream)
+            else:
+                binding.prefill(q, k, v, scale=w.scale, causal=w.causal, seqlens_k=sl, out=o,
+                                lse=lse, stream=stream)
+
+
+def W_prefill_flops(w):
+    from attention_forward_blackwell_gb300 import workloads as W
+    return W.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.d, w.causal)
+
+
+def W_decode_bytes(w, lens):
+    from attention_forward_blackwell_gb300 import workloads as W
+    return W.decode_bytes(w.Hkv, w.Hq, w.d, lens)
+
+
+def _median(xs):
+    return statistics.median(xs)
 
 
 def run_ours(args, dist):
     import torch
-    from attention_forward_blackwell_gb300 import binding, build, inputs, workloads
+    from attention_forward_blackwell_gb300 import binding, build
 
     build.build()
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     peaks = load_peaks()
-    W = workloads
-    wn, wc = W.PREFILL_D128, W.PREFILL_D128_CAUSAL
-    x = inputs.make_inputs(wn.B, wn.Hq, wn.Hkv, wn.Sq, wn.Sk, wn.d, tag=wn.tag, device=dev)
-    o_n, o_c = torch.empty_like(x.q), torch.empty_like(x.q)
-    l_n = torch.empty(wn.B, wn.Hq, wn.Sq, device=dev)
-    l_c = torch.empty_like(l_n)
+    cases = [(key, Case(w, dev, dist.world, dist.rank))
+             for key, w in bench_workloads(args.decode_batch)]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.int8, device=dev)
-    f_n = W.prefill_flops(wn.B, wn.Hq, wn.Sq, wn.Sk, wn.d, False)
-    f_c = W.prefill_flops(wc.B, wc.Hq, wc.Sq, wc.Sk, wc.d, True)
+    K = args.steps
+    W_ = max(3, args.warmup)
+    reps = max(1, math.ceil(MIN_REPS / K))
 
-    def step_nc():
-        binding.prefill(x.q, x.k, x.v, scale=wn.scale, causal=False, out=o_n, lse=l_n)
-
-    def step_c():
-        binding.prefill(x.q, x.k, x.v, scale=wc.scale, causal=True, out=o_c, lse=l_c)
-
-    for _ in range(max(3, args.warmup)):
-        flush.zero_()
-        step_nc()
-        step_c()
+    for _ in range(W_):
+        for _, c in cases:
+            flush.zero_()
+            c.run()
     torch.cuda.synchronize()
     assert binding.get_device_error() == binding.FA_OK
 
-    K = args.steps
-    ev_n, ev_c = _events(torch, K), _events(torch, K)
+    ev = {key: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K * reps)] for key, _ in cases}
     clocks = ClockSampler(dist.local_rank).start()
     time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()                    # L2 flush, outside the timed events
-        ev_n[i][0].record()
-        step_nc()
-        ev_n[i][1].record()
-        ev_c[i][0].record()
-        step_c()
-        ev_c[i][1].record()
+        for key, c in cases:
+            for r in range(reps):
+                flush.zero_()                    # L2 flush, outside the timed events
+                a, b = ev[key][i * reps + r]
+                a.record()
+                c.run()
+                b.record()
     torch.cuda.synchronize()
     dist.barrier()
     clk = clocks.stop()
-    t_n = [a.elapsed_time(b) for a, b in ev_n]
-    t_c = [a.elapsed_time(b) for a, b in ev_c]
     assert binding.get_device_error() == binding.FA_OK
-    dev_seconds = (sum(t_n) + sum(t_c)) / 1e3
-    max_seconds = dist.max(dev_seconds)
-    value = aggregate((f_n + f_c) * K, dist.world, max_seconds) / 1e12
-    ms_per_step = max_seconds * 1e3 / K
-    avg_n, avg_c = sum(t_n) / K, sum(t_c) / K
-    achieved = f_n / (avg_n * 1e-3) / 1e12
+
+    times = {key: [a.elapsed_time(b) for a, b in ev[key]] for key, _ in cases}
+    step_ms = dist.max(sum(sum(t) for t in times.values()) / K)
+    breakdown = {}
+    for key, c in cases:
+        w = c.w
+        med = dist.max(_median(times[key]))        # slowest rank's median, ms
+        rate = aggregate(c.units / dist.world, dist.world, med * 1e-3)
+        e = {"workload": w.name, "ms": round(med, 4), "reps": len(times[key]),
+             "launches_per_rep": c.launches}
+        if w.decode:
+            gbs = rate / 1e9
+            e.update({"GB_per_s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                      "algorithmic_bytes": c.units, "bound": "hbm",
+                      "sum_lengths": int(c.x.seqlens_k.sum().item())})
+        else:
+            tf = rate / 1e12
+            e.update({"TFLOPS": round(tf, 2), "frac": round(tf / peaks["bf16_tflops"], 4),
+                      "flops": c.units, "causal": w.causal, "d": w.d, "bound": "tensor"})
+            if key == "tiny_d64":
+                e["us"] = round(med * 1e3, 2)
+                e["note"] = "latency-bound (4.19 MFLOP): the roofline fraction does not apply"
+        breakdown[key] = e
+
+    head_key, head = cases[0]
+    hw = head.w
+    head_med = breakdown[head_key]["ms"]
+    value = breakdown[head_key]["TFLOPS"]
     result = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS",
-        "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill_mha_b2_h16_s4096_d128 non-causal + causal "
-                               "(one launch each per step)",
-                   "B": wn.B, "H": wn.Hq, "Sq": wn.Sq, "Sk": wn.Sk, "d": wn.d,
+        "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": dist.world, "steps": K, "warmup": W_,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+        "scaling": "strong" if dist.world > 1 else "weak",
+        "vs_baseline": round(value / PAGES_FWD_TFLOPS_B1_S8192_H16_D128, 3),
+        "vs_baseline_note": "value / 275.5 TFLOPS, the pages' forward figure for this shape on "
+                            "an RTX PRO 6000 (SM120): context, not a target",
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{hw.name} (headline); every step also runs "
+                               + ", ".join(c.w.name for _, c in cases[1:]),
+                   "B": hw.B, "H": hw.Hq, "Sq": hw.Sq, "Sk": hw.Sk, "d": hw.d, "causal": False,
                    "scale": "1/sqrt(128)", "inputs": "bf16 N(0,1), seeded",
-                   "l2": "flushed between steps (512 MiB write outside the timed events)",
-                   "parallelism": f"replica x{dist.world}"},
-        "breakdown": {
-            "noncausal_ms": round(avg_n, 4),
-            "noncausal_tflops": round(f_n / (avg_n * 1e-3) / 1e12, 2),
-            "causal_ms": round(avg_c, 4),
-            "causal_tflops": round(f_c / (avg_c * 1e-3) / 1e12, 2),
-            "context_pages_sm120_noncausal_tflops": 258.7,
-        },
-        "roofline": {"kernel": "prefill_kernel<128,false> (non-causal launch)",
-                     "bound": "tensor", "achieved": round(achieved, 2),
+                   "timing": f"median of {K * reps} launches per configuration "
+                             f"({reps} per step), CUDA events around each launch",
+                   "l2": "flushed before every timed launch (512 MiB write outside the events)",
+                   "parallelism": ("one GPU" if dist.world == 1 else
+                                   f"(batch, kv head) pairs sharded over {dist.world} ranks")},
+        "breakdown": breakdown,
+        "roofline": {"kernel": "prefill_kernel<128, non-causal> (headline launch)",
+                     "bound": "tensor", "achieved": value,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(achieved / peaks["bf16_tflops"], 4),
+                     "frac": round(value / peaks["bf16_tflops"], 4),
                      "peak_source": peaks["source"] + " (burst bf16 GEMM)",
-                     "traffic": captured_traffic("prefill"),
+                     "traffic": captured_traffic("prefill", hw.name),
                      "kernel_sources_sha256": sources_hash("prefill")[:16]},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K * reps * sum(c.launches for _, c in cases),
         "clocks": clk,
     }
-    del o_c, l_c
+    dec = breakdown["decode"]
+    dec["roofline"] = {"bound": "hbm", "achieved": dec["GB_per_s"], "peak": peaks["hbm_gbs"],
+                       "unit": "GB/s", "frac": dec["frac"], "peak_source": peaks["source"],
+                       "traffic": captured_traffic("decode", dict(cases)["decode"].w.name),
+                       "kernel_sources_sha256": sources_hash("decode")[:16]}
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, torch, binding, x, wn, f_n, f_c, dist)
-    if not args.no_decode:
-        result["decode"] = run_decode(args, torch, binding, inputs, W, peaks, dev, dist)
+        result["e2e"] = run_e2e(args, torch, head, dist)
+    del cases
+    torch.cuda.empty_cache()
     if dist.rank == 0:
-        result["cpu_baseline"] = cpu_baseline(args, wn)
+        result["cpu_baseline"] = cpu_baseline(args, hw)
     return result
 
 
-def run_e2e(args, torch, binding, x, w, f_n, f_c, dist):
-    """Same two prefill passes through the public API, fed from pinned host
-    buffers: every step copies its Q, K, V in and both passes' O and LSE out
-    inside the timed region.  The steps are pipelined the way a serving loop
+def run_e2e(args, torch, case, dist):
+    """The headline configuration through the public API, fed from pinned
+    host buffers: every step copies this rank's Q, K, V in and its O and LSE
+    out inside the timed region.  Steps are pipelined the way a serving loop
     streams batches: two device buffer sets; step i+1's inputs copy in on a
     copy stream while step i computes, and step i's outputs copy out on a
     second copy stream; events order each buffer set's reuse."""
-    hq, hk, hv = (t.cpu().pin_memory() for t in (x.q, x.k, x.v))
+    from attention_forward_blackwell_gb300 import binding
+    w = case.w
+    views = case.views
+    host_in = [[t.cpu().pin_memory() for t in v[:3]] for v in views]
     n_sets = 2
-    din = [[torch.empty_like(t) for t in (x.q, x.k, x.v)] for _ in range(n_sets)]
-    dout = [[torch.empty_like(x.q) for _ in range(2)] for _ in range(n_sets)]
-    dlse = [[torch.empty(w.B, w.Hq, w.Sq, device=x.q.device) for _ in range(2)]
-            for _ in range(n_sets)]
-    hout = [[torch.empty(x.q.shape, dtype=x.q.dtype, pin_memory=True) for _ in range(2)]
-            for _ in range(n_sets)]
-    hlse = [[torch.empty(w.B, w.Hq, w.Sq, dtype=torch.float32, pin_memory=True)
-             for _ in range(2)] for _ in range(n_sets)]
+    dev_in = [[[torch.empty_like(t) for t in v[:3]] for v in views] for _ in range(n_sets)]
+    dev_out = [[(torch.empty_like(v[4]), torch.empty_like(v[5])) for v in views]
+               for _ in range(n_sets)]
+    host_out = [[(torch.empty(v[4].shape, dtype=v[4].dtype, pin_memory=True),
+                  torch.empty(v[5].shape, dtype=v[5].dtype, pin_memory=True)) for v in views]
+                for _ in range(n_sets)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     s_comp = torch.cuda.current_stream()
-    ev = lambda: torch.cuda.Event()
-    in_done = [ev() for _ in range(n_sets)]
-    comp_done = [ev() for _ in range(n_sets)]
-    out_done = [ev() for _ in range(n_sets)]
+    in_done = [torch.cuda.Event() for _ in range(n_sets)]
+    comp_done = [torch.cuda.Event() for _ in range(n_sets)]
+    out_done = [torch.cuda.Event() for _ in range(n_sets)]
     used = [False] * n_sets
-    K = max(1, min(args.steps, 200))
+    K = max(20, min(args.steps, 200))
 
     def step(i):
         j = i % n_sets
-        dq, dk, dv = din[j]
         with torch.cuda.stream(s_in):
             if used[j]:
                 s_in.wait_event(comp_done[j])      # the set's inputs are no longer read
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
+            for hs, ds in zip(host_in, dev_in[j]):
+                for h, d in zip(hs, ds):
+                    d.copy_(h, non_blocking=True)
             in_done[j].record(s_in)
         s_comp.wait_event(in_done[j])
         if used[j]:
             s_comp.wait_event(out_done[j])         # the set's outputs have been read back
-        binding.prefill(dq, dk, dv, scale=w.scale, causal=False, out=dout[j][0],
-                        lse=dlse[j][0], stream=s_comp)
-        binding.prefill(dq, dk, dv, scale=w.scale, causal=True, out=dout[j][1],
-                        lse=dlse[j][1], stream=s_comp)
+        for (q, k, v), (o, lse), view in zip(dev_in[j], dev_out[j], views):
+            binding.prefill(q, k, v, scale=w.scale, causal=w.causal, seqlens_k=view[3], out=o,
+                            lse=lse, stream=s_comp)
         comp_done[j].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(comp_done[j])
-            for r in range(2):
-                hout[j][r].copy_(dout[j][r], non_blocking=True)
-                hlse[j][r].copy_(dlse[j][r], non_blocking=True)
+            for (o, lse), (ho, hl) in zip(dev_out[j], host_out[j]):
+                ho.copy_(o, non_blocking=True)
+                hl.copy_(lse, non_blocking=True)
             out_done[j].record(s_out)
         used[j] = True
 
@@ -385,67 +499,20 @@ def run_e2e(args, torch, binding, x, w, f_n, f_c, dist):
     b.record(s_out)
     torch.cuda.synchronize()
     secs = dist.max(a.elapsed_time(b) / 1e3)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-    d2h = sum(t.numel() * t.element_size() for t in hout[0] + hlse[0])
-    return {"value": round(aggregate((f_n + f_c) * K, dist.world, secs) / 1e12, 2),
-            "unit": "TFLOPS", "steps": K, "h2d_bytes_per_step": h2d,
+    h2d = sum(t.numel() * t.element_size() for hs in host_in for t in hs)
+    d2h = sum(t.numel() * t.element_size() for hs in host_out[0] for t in hs)
+    return {"value": round(aggregate(case.units / dist.world * K, dist.world, secs) / 1e12, 2),
+            "unit": "TFLOPS", "workload": w.name, "steps": K, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(secs * 1e3 / K, 4),
             "pipelined": "2 buffer sets; copy-in, compute and copy-out on 3 streams"}
-
-
-def run_decode(args, torch, binding, inputs, W, peaks, dev, dist):
-    w = W.DECODE
-    if args.decode_batch is not None and args.decode_batch != w.B:
-        import dataclasses
-        w = dataclasses.replace(w, B=int(args.decode_batch), name=f"{w.name}_batch{args.decode_batch}")
-    x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device=dev,
-                           lengths=w.lengths)
-    lens = x.seqlens_k.cpu().tolist()
-    nbytes = W.decode_bytes(w.Hkv, w.Hq, w.d, lens)
-    o = torch.empty_like(x.q)
-    lse = torch.empty(w.B, w.Hq, w.Sq, device=dev)
-
-    def step():
-        binding.decode(x.q, x.k, x.v, scale=w.scale, seqlens_k=x.seqlens_k, out=o, lse=lse)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    K = args.steps
-    ev = _events(torch, K)
-    dist.barrier()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.int8, device=dev)
-    for i in range(K):
-        flush.zero_()           # L2 flush outside the timed events
-        ev[i][0].record()
-        step()
-        ev[i][1].record()
-    torch.cuda.synchronize()
-    assert binding.get_device_error() == binding.FA_OK
-    t = [a.elapsed_time(b) for a, b in ev]
-    secs = dist.max(sum(t) / 1e3)
-    gbs = aggregate(nbytes * K, dist.world, secs) / 1e9
-    per_gpu = nbytes / (sum(t) / K * 1e-3) / 1e9
-    return {"workload": w.name, "value": round(gbs, 1), "unit": "GB/s",
-            "ms_per_step": round(secs * 1e3 / K, 4), "algorithmic_bytes": nbytes,
-            "sum_lengths": int(sum(lens)),
-            "roofline": {"bound": "hbm", "achieved": round(per_gpu, 1),
-                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": round(per_gpu / peaks["hbm_gbs"], 4),
-                         "peak_source": peaks["source"],
-                         "traffic": captured_traffic("decode") if w.B == W.DECODE.B else None,
-                         "kernel_sources_sha256": sources_hash("decode")[:16]},
-            "gpu_launches": 2 * K,
-            "l2": "flushed between steps (512 MiB write outside the timed events)"}
 
 
 # -------------------------------------------------------- CPU baseline ----
 
 def cpu_baseline(args, w, budget=None):
     """The fp64 oracle, as it stands, on a bounded sample of query rows of the
-    non-causal prefill workload, over all host cores; scaled to TFLOPS."""
+    headline prefill workload, over all host cores; scaled to TFLOPS."""
     import numpy as np
-    import torch
     import oracle
     from attention_forward_blackwell_gb300 import inputs
     budget = args.cpu_seconds if budget is None else budget
@@ -474,54 +541,47 @@ def cpu_baseline(args, w, budget=None):
 # ---------------------------------------------------------- reference arm ----
 
 def run_reference(args, dist):
-    """The oracle on the host cores, per step a bounded sample of the same
+    """The oracle on the host cores, per step a bounded sample of the headline
     workload, with the same metric, unit and config as our arm."""
     if dist.rank != 0:
         return None
     import numpy as np
     import oracle
     from attention_forward_blackwell_gb300 import inputs, workloads
-    wn = workloads.PREFILL_D128
-    x = inputs.make_inputs(wn.B, wn.Hq, wn.Hkv, wn.Sq, wn.Sk, wn.d, tag=wn.tag, device="cpu")
+    w = workloads.LONG_D128
+    x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device="cpu")
     qb, kb, vb = (inputs.bf16_bits(t) for t in (x.q, x.k, x.v))
     cores = os.cpu_count() or 1
-    total = wn.B * wn.Hq * wn.Sq
+    total = w.B * w.Hq * w.Sq
     rng = np.random.default_rng(11)
     # rows per step: sized so warmup + steps stay within ~2 minutes
     probe = rng.integers(0, total, size=cores)
     t0 = time.perf_counter()
-    oracle.attention_fwd(qb, kb, vb, scale=wn.scale, rows=probe, threads=cores)
+    oracle.attention_fwd(qb, kb, vb, scale=w.scale, rows=probe, threads=cores)
     per_row_s = (time.perf_counter() - t0) / len(probe)
     n_steps = args.warmup + args.steps
     rows_per_step = int(max(cores, min(total, 120.0 / n_steps / per_row_s)))
-    # causal rows see on average half the keys: sample them too
-    flops_nc = 4.0 * wn.Sk * wn.d
+    flops_per_row = 4.0 * w.Sk * w.d
     for _ in range(args.warmup):
-        oracle.attention_fwd(qb, kb, vb, scale=wn.scale, rows=rng.integers(0, total, rows_per_step),
+        oracle.attention_fwd(qb, kb, vb, scale=w.scale, rows=rng.integers(0, total, rows_per_step),
                              threads=cores)
-    flops = 0.0
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        causal = bool(i % 2)
-        rows = rng.integers(0, total, rows_per_step)
-        oracle.attention_fwd(qb, kb, vb, scale=wn.scale, causal=causal, rows=rows, threads=cores)
-        if causal:
-            flops += float(np.sum(4.0 * ((rows % wn.Sq) + 1) * wn.d))
-        else:
-            flops += flops_nc * rows_per_step
+    for _ in range(args.steps):
+        oracle.attention_fwd(qb, kb, vb, scale=w.scale, rows=rng.integers(0, total, rows_per_step),
+                             threads=cores)
     secs = time.perf_counter() - t0
-    value = flops / secs / 1e12
+    value = flops_per_row * rows_per_step * args.steps / secs / 1e12
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOPS",
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs * 1e3 / max(1, args.steps), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill_mha_b2_h16_s4096_d128 non-causal + causal",
-                   "B": wn.B, "H": wn.Hq, "Sq": wn.Sq, "Sk": wn.Sk, "d": wn.d},
+        "config": {"workload": f"{w.name} (headline)", "B": w.B, "H": w.Hq, "Sq": w.Sq,
+                   "Sk": w.Sk, "d": w.d, "causal": False},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cores,
                          "kind": "oracle",
-                         "sample": f"{rows_per_step} random query rows per step, "
-                                   "alternating non-causal and causal steps"},
+                         "sample": f"{rows_per_step} random query rows per step "
+                                   f"(all {w.Sk} keys each)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -529,41 +589,39 @@ def run_reference(args, dist):
 
 
 def run_only(args, dist):
-    """One prefill workload (workloads.ALL by name), L2 flushed before each of
-    `steps` timed launches after `warmup` untimed ones."""
+    """One workload (workloads.ALL by name), L2 flushed before each of `steps`
+    timed launches after `warmup` untimed ones."""
     import torch
-    from attention_forward_blackwell_gb300 import binding, build, inputs, workloads as W
+    from attention_forward_blackwell_gb300 import binding, build, workloads as W
 
     build.build()
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     w = {x.name: x for x in W.ALL}.get(args.only)
-    if w is None or w.Sq != w.Sk:
-        raise SystemExit(f"--only: not a prefill workload: {args.only}")
-    x = inputs.make_inputs(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, tag=w.tag, device=dev,
-                           k_scale=w.k_scale)
-    o = torch.empty_like(x.q)
-    lse = torch.empty(w.B, w.Hq, w.Sq, device=dev)
+    if w is None:
+        raise SystemExit(f"--only: unknown workload: {args.only}")
+    if w.decode and args.decode_batch is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=int(args.decode_batch))
+    c = Case(w, dev, 1, 0)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.int8, device=dev)
-
-    def step():
-        binding.prefill(x.q, x.k, x.v, scale=w.scale, causal=w.causal, out=o, lse=lse)
-
     for _ in range(max(1, args.warmup)):
         flush.zero_()
-        step()
+        c.run()
     torch.cuda.synchronize()
-    ev = _events(torch, args.steps)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     for a, b in ev:
         flush.zero_()
         a.record()
-        step()
+        c.run()
         b.record()
     torch.cuda.synchronize()
     assert binding.get_device_error() == binding.FA_OK
-    ms = sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
-    f = W.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.d, w.causal)
-    return {"only": w.name, "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 2)}
+    ms = _median([a.elapsed_time(b) for a, b in ev])
+    if w.decode:
+        return {"only": w.name, "ms": round(ms, 4), "GB_per_s": round(c.units / (ms * 1e-3) / 1e9, 1)}
+    return {"only": w.name, "ms": round(ms, 4), "tflops": round(c.units / (ms * 1e-3) / 1e12, 2)}
 
 
 def main(argv=None):
