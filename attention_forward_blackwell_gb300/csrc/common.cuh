@@ -60,6 +60,9 @@ struct PrefillArgs {
     unsigned long long* part_count;
     unsigned long long epoch;
     float scale_log2;           // scale * log2(e)
+    // The producer of CTA c prefetches into L2 the Q tiles of CTA
+    // c + q_prefetch (dispatched about one wave later), 0: none.
+    int q_prefetch;
     unsigned long long wait_limit_ns;
     // Debug trace (nullptr in normal use): one thread per role of CTA
     // `trace_block` (linear block index) records SM clock stamps.

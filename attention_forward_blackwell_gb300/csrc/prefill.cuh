@@ -99,6 +99,12 @@ struct PrefillTraits {
     // columns into it, past the tensor at its last row.)
     static constexpr bool BOX4 = (D == 256);
     static constexpr int OCH = (D_COLS + 63) / 64;     // 64-column chunks of a CTA's O
+    // Epilogue: the softmax warpgroup of a tile, idle once its last block is
+    // done, stages and stores the first EPI_SPLIT 64-column chunks of that
+    // tile's O while the correction warpgroup does the rest (and the LSE),
+    // so that the drain of O from tensor memory runs on two warpgroups.
+    // Used by the kernels where it measured faster on GB300 (see epi_split).
+    static constexpr int EPI_SPLIT = OCH / 2;
     // chunks per ring slot: one at head_dim 512 (the 128 KB Q tile leaves
     // room for five 16 KB slots only)
     static constexpr int SLOT_CH = (D == 512) ? 1 : ((NCH >= 2) ? 2 : 1);
@@ -166,6 +172,7 @@ struct PrefillAux {
                                    // to be consumed, so sharing mb_full could let
                                    // it complete two phases ahead of its reader)
     uint64_t bar_epi[T::NQ];       // staging of O_t in shared memory complete
+    uint64_t bar_epi_sm[T::NQ];    // the softmax warpgroup's part of that staging complete
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
     uint64_t bar_split_a;          // piece of a split unit: partial result written (4 warps)
@@ -306,6 +313,25 @@ __device__ __forceinline__ PrefillWork prefill_work(const PrefillArgs& a, int c)
     return w;
 }
 
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
+__device__ __forceinline__ void prefetch_q_of(const CUtensorMap* tm_q, const PrefillArgs& a,
+                                              int c2) {
+    const PrefillWork w2 = prefill_work<T, CAUSAL, WINDOW, VARLEN>(a, c2);
+    if (w2.n_max <= 0) return;
+#pragma unroll
+    for (int t = 0; t < T::NQ; ++t) {
+        const int row = (VARLEN ? w2.q0 : 0) + w2.row0 + t * T::BM;
+        const int plane = VARLEN ? w2.h : w2.b * a.Hq + w2.h;
+        if constexpr (T::BOX4) {
+#pragma unroll
+            for (int c = 0; c < T::NCH; c += 2) tma_prefetch_l2_4d(tm_q, 0, row, c, plane);
+        } else {
+#pragma unroll
+            for (int c = 0; c < T::NCH; ++c) tma_prefetch_l2_3d(tm_q, c * 64, row, plane);
+        }
+    }
+}
+
 // Copy of the P-ready barrier, rebase mailbox and value-MMA completion
 // barrier that tile t's key block j uses, and the phase parity of that block
 // on it.  With two Q tiles (NQ = 2)
@@ -332,6 +358,12 @@ template <class T>
 __device__ __forceinline__ uint32_t ring_slot(int p) { return (uint32_t)(p % T::NSLOT); }
 template <class T>
 __device__ __forceinline__ uint32_t ring_phase(int p) { return (uint32_t)((p / T::NSLOT) & 1); }
+
+// L2 prefetch of the Q tiles of the unit that CTA c2 (a later CTA of the
+// grid) will process; issued by the producer lane after its own first loads.
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
+__device__ __forceinline__ void prefetch_q_of(const CUtensorMap* tm_q, const PrefillArgs& a,
+                                              int c2);
 
 // Loads N consecutive 64-column chunks, starting at chunk c0, of the
 // 128-row tile at (row, plane) into consecutive CHUNK-byte buffers at dst
@@ -437,6 +469,9 @@ __device__ void prefill_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm
         }
         __syncwarp();
         issued = p + 1;
+        if (p == 1 && lane == 0 && a.q_prefetch > 0 &&
+            (int)blockIdx.x + a.q_prefetch < (int)gridDim.x)
+            prefetch_q_of<T, CAUSAL, WINDOW, VARLEN>(tm_q, a, (int)blockIdx.x + a.q_prefetch);
     }
     // Drain: every copy issued by this warp must have landed before the CTA
     // exits (on the normal path they all have; after an abort some may not).
@@ -671,7 +706,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 // released as soon as its four K-steps have been issued and completed.
 
 // Producer: Q once, then the pieces in consumption order.
-template <class T, bool VARLEN>
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
 __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                      const CUtensorMap* tm_v, const PrefillArgs& a,
                                      const PrefillWork& w, PrefillAux<T>* aux, uint32_t sQ,
@@ -728,6 +763,10 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
     };
     bool ok = true;
     for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(0, false, pc);
+    if (ok && lane == 0 && a.q_prefetch > 0 &&
+        (int)blockIdx.x + a.q_prefetch * T::DV_SPLIT < (int)gridDim.x)
+        prefetch_q_of<T, CAUSAL, WINDOW, VARLEN>(tm_q, a,
+                                                 (int)blockIdx.x + a.q_prefetch * T::DV_SPLIT);
     for (int j = 0; j < w.n_max && ok; ++j) {
         if (j + 1 < w.n_max)
             for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(j + 1, false, pc);
@@ -829,12 +868,118 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     __syncwarp();
 }
 
+// Stages 32-column groups [c_begin, c_end) of one Q tile's O row r as bf16
+// (O * inv_l) into the 128-byte-swizzled staging tile at `stage` (nk == 0:
+// zeros).  Called by one warpgroup (thread = row = tensor-memory lane).
+template <class T>
+__device__ __forceinline__ void stage_o_rows(uint32_t lane_base, uint32_t o_col, uint32_t stage,
+                                             int r, int nk, float inv_l, int c_begin, int c_end) {
+#pragma unroll 1
+    for (int c32 = c_begin; c32 < c_end; ++c32) {
+        uint32_t v[32];
+        if (nk > 0) {
+            tmem_ld32(lane_base + o_col + c32 * 32, v);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        const uint32_t row_addr = stage + (c32 >> 1) * T::CHUNK + r * 128;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            const int g = (c32 & 1) * 4 + g4;    // 16-byte granule within the 128-byte row
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pk[e] = pack_bf16x2(__uint_as_float(v[g4 * 8 + 2 * e]) * inv_l,
+                                    __uint_as_float(v[g4 * 8 + 2 * e + 1]) * inv_l);
+            const uint32_t addr = row_addr + ((uint32_t)(g ^ (r & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[0]),
+                         "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                         : "memory");
+        }
+    }
+}
+
+// Final normaliser of a row: the row sum l and max m (log2 units) of its
+// visible keys, plus the head's attention sink (one more term e^{sigma}
+// without a value, O rebased to max(m, sigma)).  Returns 1 / l' scaled by
+// that rebase, and sets lf / mf to the final sum and max.
+__device__ __forceinline__ float final_scale(const PrefillArgs& a, int h, float l, float m,
+                                             float& lf, float& mf) {
+    lf = l;
+    mf = m;
+    float oscale = 1.f;
+    if (a.sinks != nullptr) {
+        const float sg = a.sinks[h] * kLog2e;
+        const float m2 = fmaxf(m, sg);
+        if (m2 == -INFINITY) {
+            lf = 0.f;
+        } else {
+            oscale = (m == -INFINITY) ? 0.f : ex2_approx(m - m2);
+            lf = l * oscale + ex2_approx(sg - m2);
+            mf = m2;
+        }
+    }
+    return (lf > 0.f) ? oscale / lf : 0.f;
+}
+
+// Whether a kernel splits its epilogue between the softmax and correction
+// warpgroups: the one-tile kernels (head_dim 256, 512) and the masked
+// (causal or windowed) two-tile ones, where it measured 1-2 % faster on
+// GB300; in the unmasked two-tile kernels it measured ~1 % slower (their
+// softmax runs closer to its register budget).  Packed sequences store
+// row by row from the correction warpgroup.
+template <class T, bool MASKED, bool VARLEN>
+__host__ __device__ constexpr bool epi_split() {
+    return T::EPI_SPLIT > 0 && !VARLEN && (T::NQ == 1 || MASKED);
+}
+
+// The softmax warpgroup's part of tile t's epilogue (dense launches of
+// whole units): O chunks [0, EPI_SPLIT) staged and stored by this
+// warpgroup once the last value MMA of the tile has completed.
+template <class T, bool VARLEN, bool ENABLED>
+__device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const PrefillArgs& a,
+                                      const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
+                                      uint32_t sQ, float l, float m, const WaitCtx& wc) {
+    if constexpr (!ENABLED) {
+        return;
+    } else {
+        if (w.piece >= 0) return;   // pieces of split units: the correction writes them
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        const int r = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int nk = w.n_kv[t];
+        if (nk > 0) {
+            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, nk - 1)]), sig_par<T>(nk - 1),
+                           wc, kErrWaitTimeout | kSiteEpiPv))
+                return;
+            tc_fence_after();
+        }
+        float lf, mf;
+        const float inv_l = final_scale(a, w.h, l, m, lf, mf);
+        const uint32_t stage = sQ + t * T::QTILE;
+        stage_o_rows<T>(lane_base, T::o_col(t), stage, r, nk, inv_l, 0, 2 * T::EPI_SPLIT);
+        fence_proxy_async_smem();
+        mbar_arrive_warp(smem_u32(&aux->bar_epi_sm[t]));
+        if ((warp & 3) == 0 && lane == 0 && w.row0 + t * T::BM < a.Sq &&
+            mbar_wait_lane(smem_u32(&aux->bar_epi_sm[t]), 0, wc, kErrWaitTimeout | kSiteEpiStage)) {
+#pragma unroll
+            for (int ch = 0; ch < T::EPI_SPLIT; ++ch)
+                tma_store_3d(tm_o, stage + ch * T::CHUNK, w.dv0 + ch * 64, w.row0 + t * T::BM,
+                             w.b * a.Hq + w.h);
+            bulk_commit_group();
+            bulk_wait_group_read_0();   // the CTA may exit once shared memory was read
+        }
+    }
+}
+
 // ------------------------------------------------------------- softmax ----
 
-template <class T, bool CAUSAL, bool WINDOW>
-__device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillWork& w,
-                                     PrefillAux<T>* aux, uint32_t tmem, const WaitCtx& wc,
-                                     unsigned long long* tr) {
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
+__device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const PrefillArgs& a,
+                                     const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
+                                     uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((warp & 3) != 0 || lane != 0) tr = nullptr;
     const int trole = t == 0 ? kTrSoftmax0 : kTrSoftmax1;
@@ -955,6 +1100,8 @@ __device__ void prefill_softmax_role(int t, const PrefillArgs& a, const PrefillW
         aux->mb_l[t][r] = l_run;
         aux->mb_m[t][r] = m_run;
         mbar_arrive_warp(smem_u32(&aux->bar_fin[t]));
+        softmax_epilogue_part<T, VARLEN, epi_split<T, CAUSAL || WINDOW, VARLEN>()>(
+            t, tm_o, a, w, aux, tmem, sQ, l_run, m_run, wc);
     }
 }
 
@@ -1089,7 +1236,7 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
 // SPLIT: the instantiation can receive pieces of split units (only the
 // unmasked, unwindowed one: the work split never cuts causal or windowed
 // units, whose lengths differ); the others compile none of that code.
-template <class T, bool SPLIT, bool VARLEN>
+template <class T, bool SPLIT, bool VARLEN, bool EPI>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
                                         const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
                                         uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
@@ -1181,60 +1328,43 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             ml[T::BM + r] = (nk > 0) ? l : 0.f;
             continue;
         }
-        // attention sink: one more term e^{sigma} of the normaliser, without a
-        // value; O (accumulated in basis m) is rebased to max(m, sigma)
-        float lf = l, mf = m, oscale = 1.f;
-        if (a.sinks != nullptr) {
-            const float sg = a.sinks[w.h] * kLog2e;
-            const float m2 = fmaxf(m, sg);
-            if (m2 == -INFINITY) {
-                lf = 0.f;
-            } else {
-                oscale = (m == -INFINITY) ? 0.f : ex2_approx(m - m2);
-                lf = l * oscale + ex2_approx(sg - m2);
-                mf = m2;
-            }
-        }
-        const float inv_l = (lf > 0.f) ? oscale / lf : 0.f;
+        float lf, mf;
+        const float inv_l = final_scale(a, w.h, l, m, lf, mf);
         const uint32_t stage = sQ + t * T::QTILE;
         const int row = w.row0 + t * T::BM + r;
         // packed sequences: a tile that runs past the end of its sequence is
         // stored row by row (a TMA store would write the next sequence's rows)
         const bool direct = VARLEN && w.row0 + t * T::BM + T::BM > w.Lq;
-        constexpr int d_full = T::D_COLS * T::DV_SPLIT;
-        uint16_t* orow =
-            VARLEN ? a.o + ((size_t)(w.q0 + row) * a.Hq + w.h) * d_full + w.dv0 : nullptr;
+        // chunks [0, EPI_SPLIT) are the softmax warpgroup's when split
+        const int ch0 = (EPI && w.piece < 0) ? T::EPI_SPLIT : 0;
+        if (VARLEN && direct) {
+            constexpr int d_full = T::D_COLS * T::DV_SPLIT;
+            uint16_t* orow = a.o + ((size_t)(w.q0 + row) * a.Hq + w.h) * d_full + w.dv0;
 #pragma unroll 1
-        for (int c32 = 0; c32 < (T::D_COLS + 31) / 32; ++c32) {
-            uint32_t v[32];
-            if (nk > 0) {
-                tmem_ld32(lane_base + T::o_col(t) + c32 * 32, v);
-                tmem_wait_ld();
-            } else {
+            for (int c32 = 0; c32 < (T::D_COLS + 31) / 32; ++c32) {
+                uint32_t v[32];
+                if (nk > 0) {
+                    tmem_ld32(lane_base + T::o_col(t) + c32 * 32, v);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = 0u;
-            }
-            const int ch = c32 >> 1;                 // 64-column chunk
-            const uint32_t row_addr = stage + ch * T::CHUNK + r * 128;
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
 #pragma unroll
-            for (int g4 = 0; g4 < 4; ++g4) {
-                const int g = (c32 & 1) * 4 + g4;    // 16-byte granule within the 128-byte row
-                uint32_t pk[4];
+                for (int g4 = 0; g4 < 4; ++g4) {
+                    uint32_t pk[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    pk[e] = pack_bf16x2(__uint_as_float(v[g4 * 8 + 2 * e]) * inv_l,
-                                        __uint_as_float(v[g4 * 8 + 2 * e + 1]) * inv_l);
-                if (VARLEN && direct) {
+                    for (int e = 0; e < 4; ++e)
+                        pk[e] = pack_bf16x2(__uint_as_float(v[g4 * 8 + 2 * e]) * inv_l,
+                                            __uint_as_float(v[g4 * 8 + 2 * e + 1]) * inv_l);
                     if (row < w.Lq)
                         *reinterpret_cast<uint4*>(orow + c32 * 32 + g4 * 8) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    continue;
                 }
-                const uint32_t addr = row_addr + ((uint32_t)(g ^ (r & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[0]),
-                             "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                             : "memory");
             }
+        } else {
+            stage_o_rows<T>(lane_base, T::o_col(t), stage, r, nk, inv_l, 2 * ch0,
+                            (T::D_COLS + 31) / 32);
         }
         // (with split output columns every part has the same statistics;
         // the first part stores LSE)
@@ -1250,7 +1380,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         if (issuer && !direct && w.row0 + t * T::BM < (VARLEN ? w.Lq : a.Sq) &&
             mbar_wait_lane(smem_u32(&aux->bar_epi[t]), 0, wc, kErrWaitTimeout | kSiteEpiStage)) {
 #pragma unroll
-            for (int ch = 0; ch < T::OCH; ++ch)
+            for (int ch = ch0; ch < T::OCH; ++ch)
                 tma_store_3d(tm_o, stage + ch * T::CHUNK, w.dv0 + ch * 64,
                              (VARLEN ? w.q0 : 0) + w.row0 + t * T::BM,
                              VARLEN ? w.h : w.b * a.Hq + w.h);
@@ -1298,6 +1428,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         for (int t = 0; t < T::NQ; ++t) {
             mbar_init(smem_u32(&aux->bar_fin[t]), 4);
             mbar_init(smem_u32(&aux->bar_epi[t]), 4);
+            mbar_init(smem_u32(&aux->bar_epi_sm[t]), 4);
         }
         mbar_init(smem_u32(&aux->bar_drain[0]), 1);
         mbar_init(smem_u32(&aux->bar_drain[1]), 1);
@@ -1323,19 +1454,20 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 
     if (wg < T::NQ) {
         setmaxnreg_inc<T::template Regs<CAUSAL || WINDOW>::SOFTMAX>();
-        prefill_softmax_role<T, CAUSAL, WINDOW>(wg, args, w, aux, tmem, wc, tr);
+        prefill_softmax_role<T, CAUSAL, WINDOW, VARLEN>(wg, &tm_o, args, w, aux, tmem, sQ, wc, tr);
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
-        prefill_correction_role<T, !CAUSAL && !WINDOW && !VARLEN && T::DV_SPLIT == 1, VARLEN>(
-            &tm_o, args, w, aux, tmem, sQ, wc, tr);
+        prefill_correction_role<T, !CAUSAL && !WINDOW && !VARLEN && T::DV_SPLIT == 1, VARLEN,
+                                epi_split<T, CAUSAL || WINDOW, VARLEN>()>(&tm_o, args, w, aux,
+                                                                          tmem, sQ, wc, tr);
     } else {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
         if constexpr (T::CONSUME_ORDER) {
             if (warp == T::MMA_WARP)
                 prefill_mma_role_dv<T>(args, w, aux, tmem, sQ, sRing, wc, tr);
             else if (warp == T::LOAD_WARP)
-                prefill_load_role_dv<T, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux, sQ, sRing, wc,
-                                                tr);
+                prefill_load_role_dv<T, CAUSAL, WINDOW, VARLEN>(&tm_q, &tm_k, &tm_v, args, w, aux,
+                                                                sQ, sRing, wc, tr);
         } else {
             if (warp == T::MMA_WARP)
                 prefill_mma_role<T, VARLEN>(0, args, w, aux, tmem, sQ, sRing, wc, tr);

@@ -166,6 +166,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// Prefetch of a tile (the tensor map's box at these coordinates) into L2:
+// no shared memory, no completion; a later tiled load of the same box then
+// finds it in L2.  Coordinates past the tensor's bounds fetch nothing.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* m, int x, int y, int z,
+                                                   int w) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z), "r"(w)
+                 : "memory");
+}
+
 // 4-D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, int x, int y,
                                             int z, int w, uint32_t bar) {
