@@ -354,6 +354,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     a.trace_block = g_trace_block;
     p.head_dim = head_dim;
     p.causal = causal ? 1 : 0;
+    p.num_sms = di->num_sms;
     // work split: whole units, then the last partial wave's units in pieces
     const long long units = (long long)batch * hq * a.num_mblk;
     if (units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;

@@ -85,6 +85,7 @@ struct PrefillLaunch {
     int n_tail;                 // split units
     int head_dim;
     int causal;
+    int num_sms;                // SMs of the device (CTAs of a persistent launch)
 };
 
 // Query rows of one prefill unit (query block) for a head dimension.

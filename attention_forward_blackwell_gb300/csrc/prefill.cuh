@@ -176,6 +176,8 @@ struct PrefillAux {
     uint64_t bar_drain[2];
     uint64_t bar_tail;             // producer-private: partial last value tile landed
     uint64_t bar_split_a;          // piece of a split unit: partial result written (4 warps)
+    uint64_t bar_qfree;            // persistent: the unit's last score MMA completed (Q free)
+    uint64_t bar_odrained;         // persistent: the unit's O has been read out of tensor memory
     uint32_t tmem_base;
     int abort_flag;
     int merge_last;
@@ -189,7 +191,7 @@ struct PrefillAux {
 enum : unsigned int {
     kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
-    kSiteEpiStage, kSiteSplitA
+    kSiteEpiStage, kSiteSplitA, kSiteLoadQfree, kSiteMmaOdrained, kSiteSmOdrained
 };
 
 // Recorded if a piece's arrival could not be counted (never expected: every
@@ -705,6 +707,55 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
 // a value tile while a whole key tile waits behind it.  Each K piece is
 // released as soon as its four K-steps have been issued and completed.
 
+// Loads ring position p (then p + 1): the 64-column chunks
+// [pc SLOT_CH, (pc + 1) SLOT_CH) of K_j (is_v false) or of the CTA's part of
+// V_j.  A partial last value tile is zeroed past the sequence end before it
+// is published; `ntail` counts those copies (the parity of bar_tail).
+// Executed by the producer warp (lane 0 issues).
+template <class T, bool VARLEN>
+__device__ __forceinline__ bool load_piece(const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                           const PrefillArgs& a, const PrefillWork& w,
+                                           PrefillAux<T>* aux, uint32_t sRing, const WaitCtx& wc,
+                                           unsigned long long* tr, int j, bool is_v, int pc,
+                                           int& p, int& ntail) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t slot = ring_slot<T>(p);
+    if (!mbar_wait(smem_u32(&aux->bar_empty[slot]), ring_phase<T>(p) ^ 1u, wc,
+                   kErrWaitTimeout | kSiteLoadEmpty))
+        return false;
+    trace_mark(tr, kTrLoad, p >> 4, p & 15);   // position p's copy issued
+    const uint32_t full = smem_u32(&aux->bar_full[slot]);
+    const uint32_t dst = sRing + slot * T::SLOT;
+    const int jk = w.kb + j;
+    const int rv = w.L - jk * T::BN;
+    int ty = (VARLEN ? w.k0 : 0) + jk * T::BN, tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
+    if (a.block_table != nullptr) {
+        const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
+        ty = ty % a.page_size;
+        tz = page * a.Hkv + w.hk;
+    }
+    const int c0 = pc * T::SLOT_CH + (is_v ? w.dv0 / 64 : 0);   // first chunk of the slot
+    if (is_v && j == w.n_max - 1 && rv < T::BN) {
+        // partial last value tile: rows [rv, BN) zeroed before publication
+        const uint32_t tail = smem_u32(&aux->bar_tail);
+        if (lane == 0) {
+            mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
+            load_chunks<T, T::SLOT_CH>(dst, tm_v, c0, ty, tz, tail);
+        }
+        if (!mbar_wait(tail, (uint32_t)(ntail & 1), wc, kErrWaitTimeout | kSiteLoadTail))
+            return false;
+        ++ntail;
+        zero_value_tail<T>(dst, rv);
+        if (lane == 0) mbar_arrive(full);
+    } else if (lane == 0) {
+        mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
+        load_chunks<T, T::SLOT_CH>(dst, is_v ? tm_v : tm_k, c0, ty, tz, full);
+    }
+    __syncwarp();
+    ++p;
+    return true;
+}
+
 // Producer: Q once, then the pieces in consumption order.
 template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
 __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
@@ -723,43 +774,10 @@ __device__ void prefill_load_role_dv(const CUtensorMap* tm_q, const CUtensorMap*
         load_chunks<T, T::NCH>(sQ, tm_q, 0, (VARLEN ? w.q0 : 0) + w.row0,
                                VARLEN ? w.h : w.b * a.Hq + w.h, bar_q);
     }
-    int p = 0;   // ring position of the next piece
-    // one 64-column chunk of K_j (is_v = false) or of this CTA's part of V_j
+    int p = 0;       // ring position of the next piece
+    int ntail = 0;   // partial value pieces loaded so far
     auto load = [&](int j, bool is_v, int pc) -> bool {
-        const uint32_t slot = ring_slot<T>(p);
-        if (!mbar_wait(smem_u32(&aux->bar_empty[slot]), ring_phase<T>(p) ^ 1u, wc,
-                       kErrWaitTimeout | kSiteLoadEmpty))
-            return false;
-        trace_mark(tr, kTrLoad, p >> 4, p & 15);   // position p's copy issued
-        const uint32_t full = smem_u32(&aux->bar_full[slot]);
-        const uint32_t dst = sRing + slot * T::SLOT;
-        const int jk = w.kb + j;
-        const int rv = w.L - jk * T::BN;
-        int ty = (VARLEN ? w.k0 : 0) + jk * T::BN, tz = VARLEN ? w.hk : w.b * a.Hkv + w.hk;
-        if (a.block_table != nullptr) {
-            const int page = a.block_table[(size_t)w.b * a.max_pages + ty / a.page_size];
-            ty = ty % a.page_size;
-            tz = page * a.Hkv + w.hk;
-        }
-        const int c0 = pc * T::SLOT_CH + (is_v ? w.dv0 / 64 : 0);   // first chunk of the slot
-        if (is_v && j == w.n_max - 1 && rv < T::BN) {
-            // partial last value tile: rows [rv, BN) zeroed before publication
-            const uint32_t tail = smem_u32(&aux->bar_tail);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(tail, (uint32_t)T::SLOT);
-                load_chunks<T, T::SLOT_CH>(dst, tm_v, c0, ty, tz, tail);
-            }
-            if (!mbar_wait(tail, (uint32_t)(pc & 1), wc, kErrWaitTimeout | kSiteLoadTail))
-                return false;
-            zero_value_tail<T>(dst, rv);
-            if (lane == 0) mbar_arrive(full);
-        } else if (lane == 0) {
-            mbar_arrive_expect_tx(full, (uint32_t)T::SLOT);
-            load_chunks<T, T::SLOT_CH>(dst, is_v ? tm_v : tm_k, c0, ty, tz, full);
-        }
-        __syncwarp();
-        ++p;
-        return true;
+        return load_piece<T, VARLEN>(tm_k, tm_v, a, w, aux, sRing, wc, tr, j, is_v, pc, p, ntail);
     };
     bool ok = true;
     for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(0, false, pc);
@@ -901,6 +919,36 @@ __device__ __forceinline__ void stage_o_rows(uint32_t lane_base, uint32_t o_col,
     }
 }
 
+// Writes 32-column groups [c_begin, c_end) of one O row (O * inv_l, bf16)
+// straight to global memory at orow (nk == 0: zeros); rows past the query
+// length write nothing.
+template <class T>
+__device__ __forceinline__ void store_o_rows_direct(uint32_t lane_base, uint32_t o_col,
+                                                    uint16_t* orow, bool row_ok, int nk,
+                                                    float inv_l, int c_begin, int c_end) {
+#pragma unroll 1
+    for (int c32 = c_begin; c32 < c_end; ++c32) {
+        uint32_t v[32];
+        if (nk > 0) {
+            tmem_ld32(lane_base + o_col + c32 * 32, v);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+        }
+        if (!row_ok) continue;
+#pragma unroll
+        for (int g4 = 0; g4 < 4; ++g4) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                pk[e] = pack_bf16x2(__uint_as_float(v[g4 * 8 + 2 * e]) * inv_l,
+                                    __uint_as_float(v[g4 * 8 + 2 * e + 1]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + c32 * 32 + g4 * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+    }
+}
+
 // Final normaliser of a row: the row sum l and max m (log2 units) of its
 // visible keys, plus the head's attention sink (one more term e^{sigma}
 // without a value, O rebased to max(m, sigma)).  Returns 1 / l' scaled by
@@ -938,10 +986,10 @@ __host__ __device__ constexpr bool epi_split() {
 // The softmax warpgroup's part of tile t's epilogue (dense launches of
 // whole units): O chunks [0, EPI_SPLIT) staged and stored by this
 // warpgroup once the last value MMA of the tile has completed.
-template <class T, bool VARLEN, bool ENABLED>
+template <class T, bool VARLEN, bool ENABLED, bool PERSIST>
 __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const PrefillArgs& a,
                                       const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
-                                      uint32_t sQ, float l, float m, const WaitCtx& wc) {
+                                      uint32_t sQ, float l, float m, const WaitCtx& wc, int J0) {
     if constexpr (!ENABLED) {
         return;
     } else {
@@ -951,13 +999,26 @@ __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const Pref
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int nk = w.n_kv[t];
         if (nk > 0) {
-            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, nk - 1)]), sig_par<T>(nk - 1),
-                           wc, kErrWaitTimeout | kSiteEpiPv))
+            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, J0 + nk - 1)]),
+                           sig_par<T>(J0 + nk - 1), wc, kErrWaitTimeout | kSiteEpiPv))
                 return;
             tc_fence_after();
         }
         float lf, mf;
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
+        if constexpr (PERSIST) {
+            // persistent kernel: the Q tile's shared memory already holds the
+            // next unit's Q, so O goes to global memory straight from registers
+            const int row = w.row0 + t * T::BM + r;
+            uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
+            store_o_rows_direct<T>(lane_base, T::o_col(t), orow, row < a.Sq, nk, inv_l, 0,
+                                   2 * T::EPI_SPLIT);
+            if (nk > 0) {
+                tc_fence_before();
+                mbar_arrive_warp(smem_u32(&aux->bar_odrained));
+            }
+            return;
+        }
         const uint32_t stage = sQ + t * T::QTILE;
         stage_o_rows<T>(lane_base, T::o_col(t), stage, r, nk, inv_l, 0, 2 * T::EPI_SPLIT);
         fence_proxy_async_smem();
@@ -976,10 +1037,15 @@ __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const Pref
 
 // ------------------------------------------------------------- softmax ----
 
-template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
+// PERSIST (one Q tile, persistent kernel): the unit is one of several that
+// this CTA processes; J0 counts the key blocks of its earlier units, and the
+// barriers, mailboxes and score buffers are indexed by the CTA-wide block
+// index J0 + j.
+template <class T, bool CAUSAL, bool WINDOW, bool VARLEN, bool PERSIST = false>
 __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const PrefillArgs& a,
                                      const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
-                                     uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
+                                     uint32_t sQ, const WaitCtx& wc, unsigned long long* tr,
+                                     int J0 = 0, int kq = 0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((warp & 3) != 0 || lane != 0) tr = nullptr;
     const int trole = t == 0 ? kTrSoftmax0 : kTrSoftmax1;
@@ -998,12 +1064,13 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
     float l_run = 0.f;         // running row_sum in that basis
     bool ok = true;
     for (int j = 0; j < nk; ++j) {
-        const int sb = (T::NSBUF == 2) ? (j & 1) : 0;
+        const int J = J0 + j;   // block index over the CTA's units
+        const int sb = (T::NSBUF == 2) ? (J & 1) : 0;
         const uint32_t scol = (T::NQ == 2) ? T::s_col(t) : T::s_col(sb);
         uint32_t u[4][32];
         {
             const uint32_t bar_s = smem_u32(&aux->bar_s_full[(T::NQ == 2) ? t : sb]);
-            const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((j >> 1) & 1);
+            const uint32_t par_s = (T::NQ == 2) ? (uint32_t)(j & 1) : (uint32_t)((J >> 1) & 1);
             if (!mbar_wait(bar_s, par_s, wc, kErrWaitTimeout | kSiteSmS)) {
                 ok = false;
                 break;
@@ -1051,8 +1118,8 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         // value MMA of the last block that used the same slot (j-1 for
         // NQ = 2, j-2 for NQ = 1), which waited for the correction's arrive
         // on P-ready, made after it had read that block's message.
-        aux->mb_alpha[sig_idx<T>(t, j)][r] = alpha;
-        mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, j)]));
+        aux->mb_alpha[sig_idx<T>(t, J)][r] = alpha;
+        mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, J)]));
         trace_mark(tr, trole, j, 3);
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sl2x2 = make_float2(sl2, sl2);
@@ -1093,15 +1160,20 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]));
+        mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, J)]));
         trace_mark(tr, trole, j, 5);
     }
+    // persistent kernel: the previous unit's statistics must have been read
+    // (the correction warpgroup arrives on O-drained after reading them)
+    if (PERSIST && ok && kq > 0)
+        ok = mbar_wait(smem_u32(&aux->bar_odrained), (uint32_t)((kq - 1) & 1), wc,
+                       kErrWaitTimeout | kSiteSmOdrained);
     if (ok) {   // final row statistics for the epilogue (own slots, own barrier)
         aux->mb_l[t][r] = l_run;
         aux->mb_m[t][r] = m_run;
         mbar_arrive_warp(smem_u32(&aux->bar_fin[t]));
-        softmax_epilogue_part<T, VARLEN, epi_split<T, CAUSAL || WINDOW, VARLEN>()>(
-            t, tm_o, a, w, aux, tmem, sQ, l_run, m_run, wc);
+        softmax_epilogue_part<T, VARLEN, epi_split<T, CAUSAL || WINDOW, VARLEN>(), PERSIST>(
+            t, tm_o, a, w, aux, tmem, sQ, l_run, m_run, wc, J0);
     }
 }
 
@@ -1236,10 +1308,11 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
 // SPLIT: the instantiation can receive pieces of split units (only the
 // unmasked, unwindowed one: the work split never cuts causal or windowed
 // units, whose lengths differ); the others compile none of that code.
-template <class T, bool SPLIT, bool VARLEN, bool EPI>
+template <class T, bool SPLIT, bool VARLEN, bool EPI, bool PERSIST = false>
 __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillArgs& a,
                                         const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
-                                        uint32_t sQ, const WaitCtx& wc, unsigned long long* tr) {
+                                        uint32_t sQ, const WaitCtx& wc, unsigned long long* tr,
+                                        int J0 = 0, int k = 0) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((warp & 3) != 0 || lane != 0) tr = nullptr;
     const int r = (warp & 3) * 32 + lane;
@@ -1249,16 +1322,17 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
     for (int j = 0; j < w.n_max && ok; ++j) {
         for (int t = 0; t < T::NQ; ++t) {
             if (j >= w.n_kv[t]) continue;
-            if (!mbar_wait(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, j)]), sig_par<T>(j), wc,
+            const int J = J0 + j;   // block index over the CTA's units
+            if (!mbar_wait(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, J)]), sig_par<T>(J), wc,
                            kErrWaitTimeout | kSiteCorrMbox)) {
                 ok = false;
                 break;
             }
             trace_mark(tr, kTrCorr, j, 4 * t);
-            const float alpha = aux->mb_alpha[sig_idx<T>(t, j)][r];
+            const float alpha = aux->mb_alpha[sig_idx<T>(t, J)][r];
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
-                if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, j - 1)]), sig_par<T>(j - 1), wc,
+                if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, J - 1)]), sig_par<T>(J - 1), wc,
                                kErrWaitTimeout | kSiteCorrPv)) {
                     ok = false;
                     break;
@@ -1276,14 +1350,15 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 tmem_wait_st();
             }
             tc_fence_before();
-            mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, j)]));   // O_t safe for PV_t(j)
+            mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, J0 + j)]));   // O_t safe for PV_t(j)
             trace_mark(tr, kTrCorr, j, 4 * t + 1);
         }
     }
     // epilogue: O / row_sum -> bf16 -> shared (Q tile's space, 128-byte swizzled) -> TMA store
     for (int t = 0; t < T::NQ && ok; ++t) {
         const int nk = w.n_kv[t];
-        if (!mbar_wait(smem_u32(&aux->bar_fin[t]), 0, wc, kErrWaitTimeout | kSiteEpiMbox)) {
+        if (!mbar_wait(smem_u32(&aux->bar_fin[t]), PERSIST ? (uint32_t)(k & 1) : 0u, wc,
+                       kErrWaitTimeout | kSiteEpiMbox)) {
             ok = false;
             break;
         }
@@ -1295,8 +1370,8 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             // accumulator complete in issue order).  The wait is exact: the
             // previous PV on the same barrier copy completed before the last
             // score MMA was issued.
-            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, nk - 1)]), sig_par<T>(nk - 1), wc,
-                           kErrWaitTimeout | kSiteEpiPv)) {
+            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, J0 + nk - 1)]),
+                           sig_par<T>(J0 + nk - 1), wc, kErrWaitTimeout | kSiteEpiPv)) {
                 ok = false;
                 break;
             }
@@ -1330,6 +1405,22 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         }
         float lf, mf;
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
+        if constexpr (PERSIST) {
+            // persistent kernel: O straight from registers to global memory
+            // (the Q tile's shared memory holds the next unit's Q)
+            const int row = w.row0 + t * T::BM + r;
+            uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
+            store_o_rows_direct<T>(lane_base, T::o_col(t), orow, row < a.Sq, nk, inv_l,
+                                   EPI ? 2 * T::EPI_SPLIT : 0, (T::D_COLS + 31) / 32);
+            if (nk > 0) {
+                tc_fence_before();
+                mbar_arrive_warp(smem_u32(&aux->bar_odrained));
+            }
+            if (row < a.Sq && (T::DV_SPLIT == 1 || w.dv0 == 0))
+                a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+                    (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
+            continue;
+        }
         const uint32_t stage = sQ + t * T::QTILE;
         const int row = w.row0 + t * T::BM + r;
         // packed sequences: a tile that runs past the end of its sequence is
@@ -1490,6 +1581,327 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
                       aux->merge_unit[3], (int)threadIdx.x, T::THREADS);
 }
 
+// ------------------------------------------------ persistent (head_dim 256) ----
+//
+// One CTA per SM walks a static list of units: unit i of CTA x is in wave i
+// of the unit order, at position x in even waves and G - 1 - x in odd ones
+// (G CTAs; a snake, so that with causal units, which come heaviest first,
+// every CTA's total stays within one unit of the others').  Barriers, the
+// ring, tensor memory and the score buffers stay live from one unit to the
+// next: ring positions and key-block indices J count on over the CTA's units
+// (only units with work count: kq numbers them), so every parity below is a
+// running one.  What changes at a unit boundary:
+//   * the producer loads the next unit's Q once the unit's last score MMA
+//     has completed (bar_qfree), not once the unit is over;
+//   * O leaves tensor memory straight to global memory (no staging in the
+//     Q tile's space, which then already holds the next unit's Q), half per
+//     warpgroup, and both warpgroups arrive on bar_odrained when done;
+//   * the first value MMA of the next unit, which overwrites O, waits for
+//     bar_odrained; so does the softmax before it posts the next unit's
+//     final statistics (their mailbox is read by the correction warpgroup
+//     before it arrives);
+//   * units without keys are written (O = 0, LSE of the sink or -inf) by the
+//     correction warpgroup alone, without any signal.
+__device__ __forceinline__ int persist_unit(int i, int x, int G) {
+    return i * G + ((i & 1) ? G - 1 - x : x);
+}
+
+template <class T, bool CAUSAL, bool WINDOW>
+__device__ void prefill_load_role_persist(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                          const CUtensorMap* tm_v, const PrefillArgs& a,
+                                          PrefillAux<T>* aux, uint32_t sQ, uint32_t sRing,
+                                          const WaitCtx& wc, unsigned long long* tr) {
+    const int lane = threadIdx.x & 31;
+    if (lane != 0) tr = nullptr;
+    const int G = (int)gridDim.x, x = (int)blockIdx.x;
+    const uint32_t bar_q = smem_u32(&aux->bar_q);
+    if (lane == 0) {
+        tma_prefetch_desc(tm_q);
+        tma_prefetch_desc(tm_k);
+        tma_prefetch_desc(tm_v);
+    }
+    int p = 0, ntail = 0, kq = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+        const int u = persist_unit(i, x, G);
+        if (u >= a.n_full) break;
+        const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, false>(a, u);
+        if (w.n_max <= 0) continue;
+        auto load = [&](int j, bool is_v, int pc) -> bool {
+            return load_piece<T, false>(tm_k, tm_v, a, w, aux, sRing, wc, tr, j, is_v, pc, p,
+                                        ntail);
+        };
+        // K_0 first: its slots are free while the previous unit's last
+        // score MMA still reads Q
+        for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(0, false, pc);
+        if (!ok) break;
+        if (kq > 0 && !mbar_wait(smem_u32(&aux->bar_qfree), (uint32_t)((kq - 1) & 1), wc,
+                                 kErrWaitTimeout | kSiteLoadQfree))
+            break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
+            load_chunks<T, T::NCH>(sQ, tm_q, 0, w.row0, w.b * a.Hq + w.h, bar_q);
+            const int un = persist_unit(i + 1, x, G);   // this CTA's next unit
+            if (un < a.n_full) prefetch_q_of<T, CAUSAL, WINDOW, false>(tm_q, a, un);
+        }
+        __syncwarp();
+        ++kq;
+        for (int j = 0; j < w.n_max && ok; ++j) {
+            if (j + 1 < w.n_max)
+                for (int pc = 0; pc < T::PIECES && ok; ++pc) ok = load(j + 1, false, pc);
+            for (int pc = 0; pc < T::VPIECES && ok; ++pc) ok = load(j, true, pc);
+        }
+    }
+    // every copy issued must have landed before the CTA exits
+    if (lane == 0) {
+        if (kq > 0) mbar_wait_drain(bar_q, (uint32_t)((kq - 1) & 1), a.wait_limit_ns);
+        for (int q = p > T::NSLOT ? p - T::NSLOT : 0; q < p; ++q)
+            mbar_wait_drain(smem_u32(&aux->bar_full[ring_slot<T>(q)]), ring_phase<T>(q),
+                            a.wait_limit_ns);
+    }
+    __syncwarp();
+}
+
+// MMA issue over the CTA's units.  Block J of the CTA uses score buffer
+// J & 1; S(J) waits for PV(J - 2), the last reader of that buffer's P, also
+// across a unit boundary.
+template <class T, bool CAUSAL, bool WINDOW>
+__device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* aux, uint32_t tmem,
+                                         uint32_t sQ, uint32_t sRing, const WaitCtx& wc,
+                                         unsigned long long* tr) {
+    const int lane = threadIdx.x & 31;
+    if (lane != 0) {
+        __syncwarp();
+        return;
+    }
+    const int G = (int)gridDim.x, x = (int)blockIdx.x;
+    const uint32_t qd0 = sdesc_lo_sw128(sQ, 16);
+    const uint32_t kd0 = sdesc_lo_sw128(sRing, 16);
+    const uint32_t vd0 = sdesc_lo_sw128(sRing, T::CHUNK);
+    constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
+    int p = 0;   // ring position of the next piece (the producer's order)
+    auto next_piece = [&](unsigned site) -> bool {
+        if (!mbar_wait_lane(smem_u32(&aux->bar_full[ring_slot<T>(p)]), ring_phase<T>(p), wc,
+                            kErrWaitTimeout | site))
+            return false;
+        tc_fence_after();
+        return true;
+    };
+    auto slot_desc = [&](uint32_t d0) { return d0 + (uint32_t)((ring_slot<T>(p) * T::SLOT) >> 4); };
+    auto pv_done = [&](int J) -> bool {
+        if (J < 0) return true;
+        if (!mbar_wait_lane(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, J)]), sig_par<T>(J), wc,
+                            kErrWaitTimeout | kSiteMmaPv))
+            return false;
+        tc_fence_after();
+        return true;
+    };
+    // S(J) = Q K^T into score buffer J & 1, each K piece released once its
+    // K-steps complete
+    auto score = [&](int J, int jt) -> bool {
+        if (!pv_done(J - 2)) return false;
+        trace_mark(tr, kTrMma, jt, 0);
+        for (int pc = 0; pc < T::PIECES; ++pc) {
+            if (!next_piece(kSiteMmaK)) return false;
+            trace_mark(tr, kTrMma, jt, 1 + pc);
+            const uint32_t kd = slot_desc(kd0);
+#pragma unroll
+            for (int kin = 0; kin < T::SLOT_CH * 4; ++kin) {
+                const int kk = pc * T::SLOT_CH * 4 + kin;
+                umma_ss_lo(tmem + T::s_col(J & 1), qd0 + kstep_off(kk), kd + kstep_off(kin),
+                           idesc_s, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
+            ++p;
+        }
+        tc_commit(smem_u32(&aux->bar_s_full[J & 1]));
+        return true;
+    };
+    int J0 = 0, kq = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+        const int u = persist_unit(i, x, G);
+        if (u >= a.n_full) break;
+        const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, false>(a, u);
+        const int n = w.n_max;
+        if (n <= 0) continue;
+        if (!mbar_wait_lane(smem_u32(&aux->bar_q), (uint32_t)(kq & 1), wc,
+                            kErrWaitTimeout | kSiteMmaQ))
+            break;
+        tc_fence_after();
+        if (!score(J0, 0)) break;
+        if (n == 1) tc_commit(smem_u32(&aux->bar_qfree));
+        for (int j = 0; j < n && ok; ++j) {
+            const int J = J0 + j;
+            if (j + 1 < n) {
+                if (!score(J + 1, j + 1)) {
+                    ok = false;
+                    break;
+                }
+                if (j + 2 == n) tc_commit(smem_u32(&aux->bar_qfree));   // Q no longer read
+            }
+            if (!mbar_wait_lane(smem_u32(&aux->bar_p_ready[sig_idx<T>(0, J)]), sig_par<T>(J), wc,
+                                kErrWaitTimeout | kSiteMmaP)) {
+                ok = false;
+                break;
+            }
+            trace_mark(tr, kTrMma, j, 9);
+            tc_fence_after();
+            // the unit's first value MMA overwrites O: the previous unit's O
+            // must have been read out
+            if (j == 0 && kq > 0) {
+                if (!mbar_wait_lane(smem_u32(&aux->bar_odrained), (uint32_t)((kq - 1) & 1), wc,
+                                    kErrWaitTimeout | kSiteMmaOdrained)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            for (int nh = 0; nh < T::VPIECES; ++nh) {
+                if (!next_piece(kSiteMmaV)) {
+                    ok = false;
+                    break;
+                }
+                issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(J & 1) + 64,
+                               slot_desc(vd0), idesc_v, j == 0);
+                tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
+                ++p;
+            }
+            if (ok) tc_commit(smem_u32(&aux->bar_pv_done[sig_idx<T>(0, J)]));
+        }
+        J0 += n;
+        ++kq;
+    }
+    {
+        const uint32_t drain = smem_u32(&aux->bar_drain[0]);
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0, a.wait_limit_ns);
+    }
+    __syncwarp();
+}
+
+// A unit without keys: O = 0 and LSE = log of the sink term (or -inf), by
+// the correction warpgroup (thread = row).
+template <class T>
+__device__ void write_empty_unit(const PrefillArgs& a, const PrefillWork& w) {
+    const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
+    const int row = w.row0 + r;
+    float lf, mf;
+    const float inv_l = final_scale(a, w.h, 0.f, -INFINITY, lf, mf);
+    uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * T::D_COLS;
+    store_o_rows_direct<T>(0u, 0u, orow, row < a.Sq, 0, inv_l, 0, T::D_COLS / 32);
+    if (row < a.Sq)
+        a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+            (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
+}
+
+template <int D, bool CAUSAL, bool WINDOW>
+__global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
+    prefill_kernel_persist(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const __grid_constant__ CUtensorMap tm_o, const PrefillArgs args) {
+    using T = PrefillTraits<D>;
+    static_assert(T::NQ == 1 && T::DV_SPLIT == 1 && T::CONSUME_ORDER,
+                  "persistent kernel: one Q tile, whole output columns, ring in consumption order");
+    static_assert(sizeof(PrefillAux<T>) <= T::SMEM_AUX, "auxiliary shared block too large");
+    constexpr bool EPI = epi_split<T, CAUSAL || WINDOW, false>();
+    static_assert(EPI, "persistent kernel: both warpgroups write O");
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t sQ = (raw + 1023u) & ~1023u;
+    const uint32_t sRing = sQ + T::SMEM_Q;
+    auto* aux = reinterpret_cast<PrefillAux<T>*>(smem_raw + (sQ - raw) + T::SMEM_Q + T::SMEM_RING);
+    const int warp = threadIdx.x >> 5;
+    const int wg = warp >> 2;
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&aux->bar_q), 1);
+        for (int i = 0; i < T::NSLOT; ++i) {
+            mbar_init(smem_u32(&aux->bar_full[i]), 1);
+            mbar_init(smem_u32(&aux->bar_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&aux->bar_s_full[i]), 1);
+            mbar_init(smem_u32(&aux->bar_p_ready[i]), 8);
+            mbar_init(smem_u32(&aux->bar_mb_full[i]), 4);
+            mbar_init(smem_u32(&aux->bar_pv_done[i]), 1);
+        }
+        mbar_init(smem_u32(&aux->bar_fin[0]), 4);
+        mbar_init(smem_u32(&aux->bar_epi[0]), 4);
+        mbar_init(smem_u32(&aux->bar_epi_sm[0]), 4);
+        mbar_init(smem_u32(&aux->bar_drain[0]), 1);
+        mbar_init(smem_u32(&aux->bar_drain[1]), 1);
+        mbar_init(smem_u32(&aux->bar_tail), 1);
+        mbar_init(smem_u32(&aux->bar_split_a), 4);
+        mbar_init(smem_u32(&aux->bar_qfree), 1);
+        mbar_init(smem_u32(&aux->bar_odrained), 8);   // 4 softmax + 4 correction warps
+        aux->abort_flag = 0;
+        aux->merge_last = 0;
+        mbar_fence_init();
+    }
+    if (warp == T::MMA_WARP) {
+        tmem_alloc(smem_u32(&aux->tmem_base), T::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = aux->tmem_base;
+    const WaitCtx wc{smem_u32(&aux->abort_flag), (uint32_t)args.wait_limit_ns, args.err_word};
+    unsigned long long* tr = (FA_PREFILL_TRACE && args.trace != nullptr &&
+                              (int)blockIdx.x == args.trace_block)
+                                 ? args.trace
+                                 : nullptr;
+    const int G = (int)gridDim.x, x = (int)blockIdx.x;
+
+    if (wg == 0) {
+        setmaxnreg_inc<T::template Regs<CAUSAL || WINDOW>::SOFTMAX>();
+        int J0 = 0, kq = 0;
+        for (int i = 0;; ++i) {
+            const int u = persist_unit(i, x, G);
+            if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
+            const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, false>(args, u);
+            if (w.n_max <= 0) continue;
+            prefill_softmax_role<T, CAUSAL, WINDOW, false, true>(0, &tm_o, args, w, aux, tmem, sQ,
+                                                                 wc, tr, J0, kq);
+            J0 += w.n_max;
+            ++kq;
+        }
+    } else if (wg == T::CORR_WG) {
+        setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
+        int J0 = 0, kq = 0;
+        for (int i = 0;; ++i) {
+            const int u = persist_unit(i, x, G);
+            if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
+            const PrefillWork w = prefill_work<T, CAUSAL, WINDOW, false>(args, u);
+            if (w.n_max <= 0) {
+                write_empty_unit<T>(args, w);
+                continue;
+            }
+            prefill_correction_role<T, false, false, EPI, true>(&tm_o, args, w, aux, tmem, sQ, wc,
+                                                                tr, J0, kq);
+            J0 += w.n_max;
+            ++kq;
+        }
+    } else {
+        setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
+        if (warp == T::MMA_WARP)
+            prefill_mma_role_persist<T, CAUSAL, WINDOW>(args, aux, tmem, sQ, sRing, wc, tr);
+        else if (warp == T::LOAD_WARP)
+            prefill_load_role_persist<T, CAUSAL, WINDOW>(&tm_q, &tm_k, &tm_v, args, aux, sQ, sRing,
+                                                         wc, tr);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == T::MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+}
+
 // Host-side launch of one head-dimension instantiation.
 using PrefillKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs);
 
@@ -1504,6 +1916,23 @@ template <int D>
 cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
     using T = PrefillTraits<D>;
     const bool window = p.args.window > 0;
+    if constexpr (D == 256) {
+        // dense launches of whole units: one persistent CTA per SM
+        if (p.args.cu_seqlens_q == nullptr && p.n_tail == 0 && p.num_sms > 0 && p.args.n_full > 0) {
+            const PrefillKernelFn kern =
+                window ? (p.causal ? prefill_kernel_persist<D, true, true>
+                                   : prefill_kernel_persist<D, false, true>)
+                       : (p.causal ? prefill_kernel_persist<D, true, false>
+                                   : prefill_kernel_persist<D, false, false>);
+            cudaError_t e = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
+            if (e != cudaSuccess) return e;
+            const unsigned grid = (unsigned)min(p.args.n_full, p.num_sms);
+            kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o,
+                                                              p.args);
+            return cudaGetLastError();
+        }
+    }
     const PrefillKernelFn kern = p.args.cu_seqlens_q != nullptr
                                      ? pick_prefill_kernel<D, true>(p.causal, window)
                                      : pick_prefill_kernel<D, false>(p.causal, window);
