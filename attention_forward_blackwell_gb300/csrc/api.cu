@@ -112,10 +112,11 @@ bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows,
 // 128-byte swizzle, the same bytes as two boxes of the 3-D map.  d must be a
 // multiple of 128.
 bool encode_map4_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
-                         unsigned long long row_stride, unsigned long long plane_stride) {
+                         unsigned long long row_stride, unsigned long long plane_stride,
+                         unsigned box_rows = 128, unsigned box_chunks = 2) {
     const cuuint64_t dims[4] = {64, (cuuint64_t)rows, (cuuint64_t)(d / 64), (cuuint64_t)planes};
     const cuuint64_t strides[3] = {(cuuint64_t)row_stride, 128, (cuuint64_t)plane_stride};
-    const cuuint32_t box[4] = {64, 128, 2, 1};
+    const cuuint32_t box[4] = {64, box_rows, box_chunks, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -124,11 +125,14 @@ bool encode_map4_strided(CUtensorMap* m, const void* base, int d, long long rows
 }
 
 // Load maps of the prefill kernels: 4-D (two chunks per copy) for head_dim
-// 256, 3-D otherwise.
+// 256, 3-D otherwise.  The head_dim-256 V map copies 64 rows x all four
+// chunks at a time (the kernel's row-split value slots).
 bool prefill_load_map(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
-                      unsigned long long row_stride, unsigned long long plane_stride) {
+                      unsigned long long row_stride, unsigned long long plane_stride,
+                      bool value = false) {
     if (d == 256)
-        return encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride);
+        return value ? encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride, 64, 4)
+                     : encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride);
     return encode_map_strided(m, base, d, rows, planes, row_stride, plane_stride);
 }
 
@@ -307,16 +311,17 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
         if (!prefill_load_map(&p.tm_k, k, head_dim, page_size, planes, row_bytes,
                               row_bytes * page_size) ||
             !prefill_load_map(&p.tm_v, v, head_dim, page_size, planes, row_bytes,
-                              row_bytes * page_size))
+                              row_bytes * page_size, true))
             return FA_ERR_INVALID_ARG;
     } else if (vl) {
         if (!prefill_load_map(&p.tm_k, k, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes) ||
-            !prefill_load_map(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes))
+            !prefill_load_map(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes,
+                              true))
             return FA_ERR_INVALID_ARG;
     } else if (!prefill_load_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv, row_bytes,
                                  row_bytes * sk) ||
                !prefill_load_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv, row_bytes,
-                                 row_bytes * sk)) {
+                                 row_bytes * sk, true)) {
         return FA_ERR_INVALID_ARG;
     }
     PrefillArgs& a = p.args;

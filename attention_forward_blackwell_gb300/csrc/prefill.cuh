@@ -115,8 +115,18 @@ struct PrefillTraits {
     static constexpr int KSTEPS = D / 16;              // score MMA steps of K = 16
     // Value MMA N per instruction (head_dim 96: N = 96, i.e. one full and one
     // half 64-column chunk of the MN-major V tile; head_dim 512: one 64-column
-    // chunk, the content of one ring slot).
-    static constexpr int PV_N = (D <= 128) ? D : ((D == 512) ? 64 : 128);
+    // chunk, the content of one ring slot; head_dim 256: all 256 columns).
+    // Measured on GB300: an M = 128, K = 16 instruction occupies the tensor
+    // pipe ~80 cycles for any N up to 128 and 128 cycles at N = 256, so only
+    // N = 256 runs at the full rate.
+    static constexpr int PV_N = (D <= 128) ? D : ((D == 512) ? 64 : 256);
+    // head_dim 256: a V tile travels as two ring slots of 64 keys x 256
+    // columns (four 64-column chunks of 64 rows, 8 KB apart) instead of two
+    // slots of 128 keys x 128 columns, so that each N = 256 value MMA reads
+    // one slot, a slot is released after its four K-steps, and the value MMA
+    // starts once the first slot has landed.
+    static constexpr bool VROWS = (D == 256);
+    static constexpr int VROW_CHUNK = 64 * 128;          // one chunk of 64 rows, bytes
     static constexpr int NUM_WARPS = (NQ + 2) * 4;
     static constexpr int THREADS = NUM_WARPS * 32;
     static constexpr int CORR_WG = NQ;
@@ -402,6 +412,23 @@ __device__ __forceinline__ void zero_value_tail(uint32_t slot_addr, int rv) {
     __syncwarp();
 }
 
+// Row-split value slot (VROWS): zeroes local rows [r0, 64) of each of the
+// four 64-row chunks, then makes the writes visible to the tensor core.
+template <class T>
+__device__ __forceinline__ void zero_value_rows(uint32_t slot_addr, int r0) {
+    const int lane = threadIdx.x & 31;
+    const int granules = (64 - r0) * 8;   // 16-byte granules per chunk
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t base = slot_addr + c * T::VROW_CHUNK + r0 * 128;
+        for (int g = lane; g < granules; g += 32)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(base + g * 16), "r"(0)
+                         : "memory");
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+}
+
 // ------------------------------------------------------------ producer ----
 
 template <class T, bool CAUSAL, bool WINDOW, bool VARLEN>
@@ -521,6 +548,19 @@ __device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, ui
     for (int kk = 0; kk < T::BN / 16; ++kk)
         umma_ts_lo(tmem_o, tmem_p + kk * 8, vd + (uint32_t)((kk * 2048) >> 4), idesc,
                    (!first || kk > 0) ? 1u : 0u);
+}
+
+// Value MMA over a row-split V slot (VROWS): keys [64 h, 64 h + 64) of the
+// block, all PV_N output columns, 4 steps of 16 keys; the slot holds four
+// 64-row chunks (VROW_CHUNK apart, the descriptor's leading byte offset),
+// 2048 bytes per step.
+template <class T>
+__device__ __forceinline__ void issue_value_rows(uint32_t tmem_o, uint32_t tmem_p, int h,
+                                                 uint32_t vd, uint32_t idesc, bool first) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        umma_ts_lo(tmem_o, tmem_p + (h * 4 + kk) * 8, vd + (uint32_t)((kk * 2048) >> 4), idesc,
+                   (!first || h > 0 || kk > 0) ? 1u : 0u);
 }
 
 // MMA issue: one elected lane of one warp issues every tcgen05.mma of the CTA
@@ -734,6 +774,26 @@ __device__ __forceinline__ bool load_piece(const CUtensorMap* tm_k, const CUtens
         ty = ty % a.page_size;
         tz = page * a.Hkv + w.hk;
     }
+    if (T::VROWS && is_v) {
+        // keys [64 pc, 64 pc + 64) of V_j, all 256 columns (one 4-D copy of
+        // four 64-row chunks); rows past the sequence end zeroed
+        const int r0 = rv - 64 * pc;
+        const uint32_t bar = (r0 < 64) ? smem_u32(&aux->bar_tail) : full;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bar, (uint32_t)T::SLOT);
+            tma_load_4d(dst, tm_v, 0, ty + 64 * pc, 0, tz, bar);
+        }
+        if (r0 < 64) {
+            if (!mbar_wait(bar, (uint32_t)(ntail & 1), wc, kErrWaitTimeout | kSiteLoadTail))
+                return false;
+            ++ntail;
+            zero_value_rows<T>(dst, r0 > 0 ? r0 : 0);
+            if (lane == 0) mbar_arrive(full);
+        }
+        __syncwarp();
+        ++p;
+        return true;
+    }
     const int c0 = pc * T::SLOT_CH + (is_v ? w.dv0 / 64 : 0);   // first chunk of the slot
     if (is_v && j == w.n_max - 1 && rv < T::BN) {
         // partial last value tile: rows [rv, BN) zeroed before publication
@@ -815,6 +875,7 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
     const uint32_t qd0 = sdesc_lo_sw128(sQ, 16);
     const uint32_t kd0 = sdesc_lo_sw128(sRing, 16);
     const uint32_t vd0 = sdesc_lo_sw128(sRing, T::CHUNK);
+    const uint32_t vd0r = sdesc_lo_sw128(sRing, T::VROW_CHUNK);   // row-split V slots
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
     int p = 0;   // ring position of the next piece (the producer's order)
@@ -870,8 +931,12 @@ __device__ void prefill_mma_role_dv(const PrefillArgs& a, const PrefillWork& w,
                     break;
                 }
                 trace_mark(tr, kTrMma, j, 10 + nh);   // V piece nh landed
-                issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(j & 1) + 64,
-                               slot_desc(vd0), idesc_v, j == 0);
+                if constexpr (T::VROWS)
+                    issue_value_rows<T>(tmem + T::o_col(0), tmem + T::s_col(j & 1) + 64, nh,
+                                        slot_desc(vd0r), idesc_v, j == 0);
+                else
+                    issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(j & 1) + 64,
+                                   slot_desc(vd0), idesc_v, j == 0);
                 tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
                 ++p;
             }
@@ -1075,14 +1140,14 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
                 ok = false;
                 break;
             }
-            trace_mark(tr, trole, j, 0);
-            trace_mark(tr, trole, j, 1);
+            trace_mark(tr, trole, J, 0);
+            trace_mark(tr, trole, J, 1);
             tc_fence_after();
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + scol + q * 32, u[q]);
         }
         tmem_wait_ld();
-        trace_mark(tr, trole, j, 2);
+        trace_mark(tr, trole, J, 2);
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
@@ -1120,7 +1185,7 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         // on P-ready, made after it had read that block's message.
         aux->mb_alpha[sig_idx<T>(t, J)][r] = alpha;
         mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, J)]));
-        trace_mark(tr, trole, j, 3);
+        trace_mark(tr, trole, J, 3);
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 nbase = make_float2(-base, -base);
@@ -1155,13 +1220,13 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
         const float2 rsum = fadd2(rs01, rs23);
         l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
-        trace_mark(tr, trole, j, 4);
+        trace_mark(tr, trole, J, 4);
         if (kUsePolyExp2 && warp_masked) tmem_st32(lane_base + scol + 64, pk[0]);
         tmem_st32(lane_base + scol + 96, pk[1]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, J)]));
-        trace_mark(tr, trole, j, 5);
+        trace_mark(tr, trole, J, 5);
     }
     // persistent kernel: the previous unit's statistics must have been read
     // (the correction warpgroup arrives on O-drained after reading them)
@@ -1328,7 +1393,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                 ok = false;
                 break;
             }
-            trace_mark(tr, kTrCorr, j, 4 * t);
+            trace_mark(tr, kTrCorr, J0 + j, 4 * t);
             const float alpha = aux->mb_alpha[sig_idx<T>(t, J)][r];
             if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
                 // O_t must hold PV_t(j-1) before it is rebased
@@ -1351,7 +1416,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             }
             tc_fence_before();
             mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, J0 + j)]));   // O_t safe for PV_t(j)
-            trace_mark(tr, kTrCorr, j, 4 * t + 1);
+            trace_mark(tr, kTrCorr, J0 + j, 4 * t + 1);
         }
     }
     // epilogue: O / row_sum -> bf16 -> shared (Q tile's space, 128-byte swizzled) -> TMA store
@@ -1362,7 +1427,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             ok = false;
             break;
         }
-        trace_mark(tr, kTrCorr, w.n_max, 4 * t);
+        trace_mark(tr, kTrCorr, J0 + w.n_max, 4 * t + 2);
         const float l = aux->mb_l[t][r];
         const float m = aux->mb_m[t][r];
         if (nk > 0) {
@@ -1477,7 +1542,7 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
                              VARLEN ? w.h : w.b * a.Hq + w.h);
             bulk_commit_group();
         }
-        trace_mark(tr, kTrCorr, w.n_max, 4 * t + 1);
+        trace_mark(tr, kTrCorr, J0 + w.n_max, 4 * t + 3);
     }
     // the CTA may exit once the O stores have read shared memory
     if (issuer) bulk_wait_group_read_0();
@@ -1678,6 +1743,7 @@ __device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* au
     const uint32_t qd0 = sdesc_lo_sw128(sQ, 16);
     const uint32_t kd0 = sdesc_lo_sw128(sRing, 16);
     const uint32_t vd0 = sdesc_lo_sw128(sRing, T::CHUNK);
+    const uint32_t vd0r = sdesc_lo_sw128(sRing, T::VROW_CHUNK);   // row-split V slots
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_v = idesc_bf16_f32(128, T::PV_N, false, true);
     int p = 0;   // ring position of the next piece (the producer's order)
@@ -1699,12 +1765,12 @@ __device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* au
     };
     // S(J) = Q K^T into score buffer J & 1, each K piece released once its
     // K-steps complete
-    auto score = [&](int J, int jt) -> bool {
+    auto score = [&](int J) -> bool {
         if (!pv_done(J - 2)) return false;
-        trace_mark(tr, kTrMma, jt, 0);
+        trace_mark(tr, kTrMma, J, 0);
         for (int pc = 0; pc < T::PIECES; ++pc) {
             if (!next_piece(kSiteMmaK)) return false;
-            trace_mark(tr, kTrMma, jt, 1 + pc);
+            trace_mark(tr, kTrMma, J, 1 + pc);
             const uint32_t kd = slot_desc(kd0);
 #pragma unroll
             for (int kin = 0; kin < T::SLOT_CH * 4; ++kin) {
@@ -1730,12 +1796,12 @@ __device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* au
                             kErrWaitTimeout | kSiteMmaQ))
             break;
         tc_fence_after();
-        if (!score(J0, 0)) break;
+        if (!score(J0)) break;
         if (n == 1) tc_commit(smem_u32(&aux->bar_qfree));
         for (int j = 0; j < n && ok; ++j) {
             const int J = J0 + j;
             if (j + 1 < n) {
-                if (!score(J + 1, j + 1)) {
+                if (!score(J + 1)) {
                     ok = false;
                     break;
                 }
@@ -1746,7 +1812,7 @@ __device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* au
                 ok = false;
                 break;
             }
-            trace_mark(tr, kTrMma, j, 9);
+            trace_mark(tr, kTrMma, J, 9);
             tc_fence_after();
             // the unit's first value MMA overwrites O: the previous unit's O
             // must have been read out
@@ -1763,8 +1829,9 @@ __device__ void prefill_mma_role_persist(const PrefillArgs& a, PrefillAux<T>* au
                     ok = false;
                     break;
                 }
-                issue_value<T>(tmem + T::o_col(0) + nh * T::PV_N, tmem + T::s_col(J & 1) + 64,
-                               slot_desc(vd0), idesc_v, j == 0);
+                trace_mark(tr, kTrMma, J, 10 + nh);
+                issue_value_rows<T>(tmem + T::o_col(0), tmem + T::s_col(J & 1) + 64, nh,
+                                    slot_desc(vd0r), idesc_v, j == 0);
                 tc_commit(smem_u32(&aux->bar_empty[ring_slot<T>(p)]));
                 ++p;
             }
