@@ -164,6 +164,16 @@ struct PrefillTraits {
     __device__ static constexpr uint32_t o_col(int t) {
         return (NQ == 2) ? (uint32_t)(256 + t * 128) : 256u;
     }
+    // head_dim 64: O_t takes 64 of its 128 columns, so P_t (64 columns of
+    // bf16 pairs) gets the other 64 instead of the upper half of S_t.  The
+    // score MMA of block j+1 then only waits for the softmax to have read
+    // S_t(j) (P-ready), not for the value MMA of block j, which runs after
+    // it; the softmax waits for that value MMA before it overwrites P_t.
+    static constexpr bool SEP_P = (D == 64);
+    __device__ static constexpr uint32_t p_col(int t) {
+        return SEP_P ? o_col(t) + 64u : s_col(t) + 64u;
+    }
+    static_assert(!SEP_P || (NQ == 2 && D_COLS <= 64), "separate P columns need room beside O");
 };
 
 template <class T>
@@ -201,7 +211,7 @@ struct PrefillAux {
 enum : unsigned int {
     kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
-    kSiteEpiStage, kSiteSplitA, kSiteLoadQfree, kSiteMmaOdrained, kSiteSmOdrained
+    kSiteEpiStage, kSiteSplitA, kSiteLoadQfree, kSiteMmaOdrained, kSiteSmOdrained, kSiteSmPv
 };
 
 // Recorded if a piece's arrival could not be counted (never expected: every
@@ -644,8 +654,24 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                     }
                     trace_mark(tr, kTrMma, j, 1 + 3 * t);
                     tc_fence_after();
+                    if constexpr (T::SEP_P) {
+                        // S_t(j+1) first (the softmax has read S_t(j)), then
+                        // PV_t(j) from the tile's own P columns
+                        if (j + 1 < w.n_kv[t]) {
+                            if (!k_next_ready) {
+                                if (!wait_tile(posK, kSiteMmaK)) { ok = false; break; }
+                                k_next_ready = true;
+                                trace_mark(tr, kTrMma, j, 7);
+                                kdesc(posK, kd);
+                            }
+                            tc_fence_after();
+                            issue_score<T>(tmem + T::s_col(t), qdesc(t), kd, idesc_s);
+                            tc_commit(smem_u32(&aux->bar_s_full[t]));
+                            trace_mark(tr, kTrMma, j, 9 + t);
+                        }
+                    }
                     if (leader) {
-                        issue_value<T>(tmem + T::o_col(t), tmem + T::s_col(t) + 64,
+                        issue_value<T>(tmem + T::o_col(t), tmem + T::p_col(t),
                                        vd0 + slot_off(posV), idesc_v, j == 0);
                         tc_commit(smem_u32(&aux->bar_pv_done[t]));
                     }
@@ -654,7 +680,7 @@ __device__ void prefill_mma_role(int tq, const PrefillArgs& a, const PrefillWork
                     // sequence may end inside tile 0)
                     if (t == 1 || (VARLEN && j >= w.n_kv[1])) release_tile(posV, false);
                     trace_mark(tr, kTrMma, j, 2 + 3 * t);
-                    if (j + 1 < w.n_kv[t]) {
+                    if (!T::SEP_P && j + 1 < w.n_kv[t]) {
                         if (!k_next_ready) {
                             if (!wait_tile(posK, kSiteMmaK)) { ok = false; break; }
                             k_next_ready = true;
@@ -1186,6 +1212,17 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         aux->mb_alpha[sig_idx<T>(t, J)][r] = alpha;
         mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sig_idx<T>(t, J)]));
         trace_mark(tr, trole, J, 3);
+        // P(j) columns: the upper half of the score buffer, or (SEP_P) the
+        // tile's own P columns, which PV_t(j-1) may still be reading
+        const uint32_t pcol = T::SEP_P ? T::p_col(t) : scol + 64;
+        if (T::SEP_P && j > 0) {
+            if (!mbar_wait(smem_u32(&aux->bar_pv_done[sig_idx<T>(t, J - 1)]), sig_par<T>(J - 1), wc,
+                           kErrWaitTimeout | kSiteSmPv)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+        }
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 nbase = make_float2(-base, -base);
@@ -1214,15 +1251,15 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
                 pk[c >> 5][c & 31] = pack_bf16x2(p.x, p.y);
                 // keys 0..63 go to columns 64..95, whose scores are already in
                 // registers: store them early to shorten the live range
-                if (c == 31) tmem_st32(lane_base + scol + 64, pk[0]);
+                if (c == 31) tmem_st32(lane_base + pcol, pk[0]);
             }
         }
         const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
         const float2 rsum = fadd2(rs01, rs23);
         l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
         trace_mark(tr, trole, J, 4);
-        if (kUsePolyExp2 && warp_masked) tmem_st32(lane_base + scol + 64, pk[0]);
-        tmem_st32(lane_base + scol + 96, pk[1]);
+        if (kUsePolyExp2 && warp_masked) tmem_st32(lane_base + pcol, pk[0]);
+        tmem_st32(lane_base + pcol + 32, pk[1]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive_warp(smem_u32(&aux->bar_p_ready[sig_idx<T>(t, J)]));
