@@ -125,14 +125,16 @@ bool encode_map4_strided(CUtensorMap* m, const void* base, int d, long long rows
 }
 
 // Load maps of the prefill kernels: 4-D (two chunks per copy) for head_dim
-// 256, 3-D otherwise.  The head_dim-256 V map copies 64 rows x all four
-// chunks at a time (the kernel's row-split value slots).
+// 256, 3-D otherwise.  The V maps of head_dim 256 and 512 copy 64 / 32 rows
+// x four 64-column chunks at a time (the kernels' row-split value slots).
 bool prefill_load_map(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
                       unsigned long long row_stride, unsigned long long plane_stride,
                       bool value = false) {
     if (d == 256)
         return value ? encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride, 64, 4)
                      : encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride);
+    if (d == 512 && value)
+        return encode_map4_strided(m, base, d, rows, planes, row_stride, plane_stride, 32, 4);
     return encode_map_strided(m, base, d, rows, planes, row_stride, plane_stride);
 }
 

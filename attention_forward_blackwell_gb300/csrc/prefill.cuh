@@ -115,18 +115,21 @@ struct PrefillTraits {
     static constexpr int KSTEPS = D / 16;              // score MMA steps of K = 16
     // Value MMA N per instruction (head_dim 96: N = 96, i.e. one full and one
     // half 64-column chunk of the MN-major V tile; head_dim 512: one 64-column
-    // chunk, the content of one ring slot; head_dim 256: all 256 columns).
-    // Measured on GB300: an M = 128, K = 16 instruction occupies the tensor
-    // pipe ~80 cycles for any N up to 128 and 128 cycles at N = 256, so only
-    // N = 256 runs at the full rate.
-    static constexpr int PV_N = (D <= 128) ? D : ((D == 512) ? 64 : 256);
-    // head_dim 256: a V tile travels as two ring slots of 64 keys x 256
-    // columns (four 64-column chunks of 64 rows, 8 KB apart) instead of two
-    // slots of 128 keys x 128 columns, so that each N = 256 value MMA reads
-    // one slot, a slot is released after its four K-steps, and the value MMA
-    // starts once the first slot has landed.
-    static constexpr bool VROWS = (D == 256);
-    static constexpr int VROW_CHUNK = 64 * 128;          // one chunk of 64 rows, bytes
+    // chunk, the content of one ring slot; head_dim 256 and 512: all 256
+    // columns of the CTA's O).  Measured on GB300: an M = 128, K = 16
+    // instruction occupies the tensor pipe ~80 cycles for any N up to 128
+    // and 128 cycles at N = 256, so only N = 256 runs at the full rate.
+    static constexpr int PV_N = (D <= 128) ? D : 256;
+    // head_dim 256 / 512: a V tile (the CTA's 256 columns of it) travels as
+    // ring slots of VROW_KEYS keys x 256 columns (four 64-column chunks of
+    // VROW_KEYS rows, VROW_CHUNK bytes apart: 64 keys in 32 KB slots at 256,
+    // 32 keys in 16 KB slots at 512) instead of slots of 128 keys x 128 or
+    // 64 columns, so that each N = 256 value MMA reads one slot, a slot is
+    // released after its K-steps, and the value MMA starts once the first
+    // slot has landed.
+    static constexpr bool VROWS = (D >= 256);
+    static constexpr int VROW_KEYS = (D == 512) ? 32 : 64;
+    static constexpr int VROW_CHUNK = VROW_KEYS * 128;   // one chunk of VROW_KEYS rows, bytes
     static constexpr int NUM_WARPS = (NQ + 2) * 4;
     static constexpr int THREADS = NUM_WARPS * 32;
     static constexpr int CORR_WG = NQ;
@@ -159,6 +162,9 @@ struct PrefillTraits {
     static_assert(DV_SPLIT == 1 ? VPIECES == PIECES : NQ == 1,
                   "split output columns only with one Q tile per CTA");
     static_assert(SMEM_TOTAL <= 232448, "shared memory per CTA exceeds the sm_103 limit");
+    static_assert(!VROWS || (4 * VROW_CHUNK == SLOT && VPIECES * VROW_KEYS == BN &&
+                             D_COLS == 256),
+                  "a row-split V slot holds VROW_KEYS keys of the CTA's 256 columns");
 
     __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * 128); }
     __device__ static constexpr uint32_t o_col(int t) {
@@ -422,12 +428,12 @@ __device__ __forceinline__ void zero_value_tail(uint32_t slot_addr, int rv) {
     __syncwarp();
 }
 
-// Row-split value slot (VROWS): zeroes local rows [r0, 64) of each of the
-// four 64-row chunks, then makes the writes visible to the tensor core.
+// Row-split value slot (VROWS): zeroes local rows [r0, VROW_KEYS) of each of
+// the four chunks, then makes the writes visible to the tensor core.
 template <class T>
 __device__ __forceinline__ void zero_value_rows(uint32_t slot_addr, int r0) {
     const int lane = threadIdx.x & 31;
-    const int granules = (64 - r0) * 8;   // 16-byte granules per chunk
+    const int granules = (T::VROW_KEYS - r0) * 8;   // 16-byte granules per chunk
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const uint32_t base = slot_addr + c * T::VROW_CHUNK + r0 * 128;
@@ -560,16 +566,17 @@ __device__ __forceinline__ void issue_value(uint32_t tmem_o, uint32_t tmem_p, ui
                    (!first || kk > 0) ? 1u : 0u);
 }
 
-// Value MMA over a row-split V slot (VROWS): keys [64 h, 64 h + 64) of the
-// block, all PV_N output columns, 4 steps of 16 keys; the slot holds four
-// 64-row chunks (VROW_CHUNK apart, the descriptor's leading byte offset),
+// Value MMA over a row-split V slot (VROWS): keys [VROW_KEYS h, +VROW_KEYS)
+// of the block, all PV_N output columns, steps of 16 keys; the slot holds
+// four chunks (VROW_CHUNK apart, the descriptor's leading byte offset),
 // 2048 bytes per step.
 template <class T>
 __device__ __forceinline__ void issue_value_rows(uint32_t tmem_o, uint32_t tmem_p, int h,
                                                  uint32_t vd, uint32_t idesc, bool first) {
+    constexpr int STEPS = T::VROW_KEYS / 16;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-        umma_ts_lo(tmem_o, tmem_p + (h * 4 + kk) * 8, vd + (uint32_t)((kk * 2048) >> 4), idesc,
+    for (int kk = 0; kk < STEPS; ++kk)
+        umma_ts_lo(tmem_o, tmem_p + (h * STEPS + kk) * 8, vd + (uint32_t)((kk * 2048) >> 4), idesc,
                    (!first || h > 0 || kk > 0) ? 1u : 0u);
 }
 
@@ -801,15 +808,16 @@ __device__ __forceinline__ bool load_piece(const CUtensorMap* tm_k, const CUtens
         tz = page * a.Hkv + w.hk;
     }
     if (T::VROWS && is_v) {
-        // keys [64 pc, 64 pc + 64) of V_j, all 256 columns (one 4-D copy of
-        // four 64-row chunks); rows past the sequence end zeroed
-        const int r0 = rv - 64 * pc;
-        const uint32_t bar = (r0 < 64) ? smem_u32(&aux->bar_tail) : full;
+        // keys [VROW_KEYS pc, +VROW_KEYS) of V_j, the CTA's 256 columns (one
+        // 4-D copy of four chunks); rows past the sequence end zeroed
+        constexpr int RK = T::VROW_KEYS;
+        const int r0 = rv - RK * pc;
+        const uint32_t bar = (r0 < RK) ? smem_u32(&aux->bar_tail) : full;
         if (lane == 0) {
             mbar_arrive_expect_tx(bar, (uint32_t)T::SLOT);
-            tma_load_4d(dst, tm_v, 0, ty + 64 * pc, 0, tz, bar);
+            tma_load_4d(dst, tm_v, 0, ty + RK * pc, w.dv0 / 64, tz, bar);
         }
-        if (r0 < 64) {
+        if (r0 < RK) {
             if (!mbar_wait(bar, (uint32_t)(ntail & 1), wc, kErrWaitTimeout | kSiteLoadTail))
                 return false;
             ++ntail;
