@@ -62,8 +62,8 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("6ba2a761abb15ac241ac2efe7f64487ac98d5e2d2f44628128000fdc935f584b",
-                "long_prefill_b1_h16_s8192_d128", 120440320),
+    "prefill": ("adea8be56ed277df78db15a1c82f1867c4184c9dda274217e10e3676350aba47",
+                "long_prefill_b1_h16_s8192_d128", 120432128),
     # captured at batch 16 (463.38 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
     "decode": ("79e7d7158f673c9efdb21fe2730b9739c7ce55f296f7439f1974e90901f86ec3",
