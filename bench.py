@@ -66,8 +66,8 @@ CAPTURED_TRAFFIC = {
                 "long_prefill_b1_h16_s8192_d128", 120432128),
     # captured at batch 16 (463.38 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
-    "decode": ("79e7d7158f673c9efdb21fe2730b9739c7ce55f296f7439f1974e90901f86ec3",
-               "decode_gqa_b64_hq64_hkv8_d128", 2204106190),
+    "decode": ("e51ed49de5a09e0690ddbd22b2e0aee632ee78e4c8991fd3922b1612478162ee",
+               "decode_gqa_b64_hq64_hkv8_d128", 2203956415),
 }
 
 
