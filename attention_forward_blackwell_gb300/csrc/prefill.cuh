@@ -158,7 +158,11 @@ struct PrefillTraits {
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
-    static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX;
+    // head_dim 256 (persistent kernel): a 2 KB O staging area for
+    // each of the softmax and correction warps (epilogue stores, see
+    // store_o_rows_staged)
+    static constexpr int SMEM_STAGE = (D == 256) ? 8 * 2048 : 0;
+    static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX + SMEM_STAGE;
     static_assert(DV_SPLIT == 1 ? VPIECES == PIECES : NQ == 1,
                   "split output columns only with one Q tile per CTA");
     static_assert(SMEM_TOTAL <= 232448, "shared memory per CTA exceeds the sm_103 limit");
@@ -230,6 +234,15 @@ constexpr unsigned int kErrSplitCount = 0x2001u;
 __device__ __forceinline__ void trace_mark(unsigned long long* tr, int role, int j, int e) {
     if (FA_PREFILL_TRACE && tr != nullptr && j * kTraceEvents + e < kTraceSlots)
         tr[role * kTraceSlots + j * kTraceEvents + e] = (unsigned long long)clock64();
+}
+
+// Debug trace stamp by the first thread of the calling warpgroup, for code
+// that has no trace pointer of its own (compiled in only with
+// FA_PREFILL_TRACE=1).
+__device__ __forceinline__ void trace_wg(const PrefillArgs& a, int role, int j, int e) {
+    if (FA_PREFILL_TRACE && a.trace != nullptr && (int)blockIdx.x == a.trace_block &&
+        (threadIdx.x & 127) == 0 && j * kTraceEvents + e < kTraceSlots)
+        a.trace[role * kTraceSlots + j * kTraceEvents + e] = (unsigned long long)clock64();
 }
 
 // Per-CTA work coordinates, computed identically by every thread.
@@ -1048,6 +1061,75 @@ __device__ __forceinline__ void store_o_rows_direct(uint32_t lane_base, uint32_t
     }
 }
 
+// The 2 KB O staging area of warp `warp` (softmax and correction warps
+// 0..7 of a one-tile kernel), after the barrier block.
+template <class T>
+__device__ __forceinline__ uint32_t stage_of(uint32_t sQ, int warp) {
+    return sQ + T::SMEM_Q + T::SMEM_RING + T::SMEM_AUX + (uint32_t)(warp & 7) * 2048u;
+}
+
+// Writes 32-column groups [c_begin, c_end) of the calling warp's 32 O rows
+// (O * inv_l, bf16; nk == 0: zeros) through the warp's 2 KB staging area at
+// `stage`.  NG groups are read from tensor memory per wait (the load latency
+// dominates otherwise); then, group by group, each lane writes its row's 64
+// bytes (16-byte chunks XOR-swizzled by row pair, 4-way bank conflicts at
+// most) and each store instruction writes 8 rows x 64 contiguous bytes (4
+// lanes per row) instead of 32 scattered 16-byte pieces.  obase: the warp's
+// first row at its first column; rows past nvalid are not written.
+template <class T, int NG>
+__device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t o_col,
+                                                    uint16_t* obase, size_t row_stride,
+                                                    int nvalid, int nk, float inv_l,
+                                                    int c_begin, int c_end, uint32_t stage) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll 1
+    for (int cb = c_begin; cb < c_end; cb += NG) {
+        uint32_t v[NG][32];
+        if (nk > 0) {
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+                if (cb + g < c_end) tmem_ld32(lane_base + o_col + (cb + g) * 32, v[g]);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int g = 0; g < NG; ++g)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) v[g][e] = 0u;
+        }
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+            const int c32 = cb + g;
+            if (c32 >= c_end) break;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    pk[e] = pack_bf16x2(__uint_as_float(v[g][i * 8 + 2 * e]) * inv_l,
+                                        __uint_as_float(v[g][i * 8 + 2 * e + 1]) * inv_l);
+                const uint32_t dst = stage + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[0]),
+                             "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                             : "memory");
+            }
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rr = 8 * k + (lane >> 2), c = lane & 3;
+                uint32_t x0, x1, x2, x3;
+                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(x0), "=r"(x1), "=r"(x2), "=r"(x3)
+                             : "r"(stage + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4))
+                             : "memory");
+                if (rr < nvalid)
+                    *reinterpret_cast<uint4*>(obase + (size_t)rr * row_stride + c32 * 32 + c * 8) =
+                        make_uint4(x0, x1, x2, x3);
+            }
+            __syncwarp();
+        }
+    }
+}
+
 // Final normaliser of a row: the row sum l and max m (log2 units) of its
 // visible keys, plus the head's attention sink (one more term e^{sigma}
 // without a value, O rebased to max(m, sigma)).  Returns 1 / l' scaled by
@@ -1107,11 +1189,14 @@ __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const Pref
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
         if constexpr (PERSIST) {
             // persistent kernel: the Q tile's shared memory already holds the
-            // next unit's Q, so O goes to global memory straight from registers
-            const int row = w.row0 + t * T::BM + r;
-            uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
-            store_o_rows_direct<T>(lane_base, T::o_col(t), orow, row < a.Sq, nk, inv_l, 0,
-                                   2 * T::EPI_SPLIT);
+            // next unit's Q, so O goes out through the warp's staging area
+            const int wrow = w.row0 + t * T::BM + (warp & 3) * 32;   // the warp's first row
+            uint16_t* obase = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + wrow) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
+            trace_wg(a, kTrSoftmax0, J0 + nk - 1, 6);
+            store_o_rows_staged<T, 4>(lane_base, T::o_col(t), obase, T::D_COLS * T::DV_SPLIT,
+                                      a.Sq - wrow, nk, inv_l, 0, 2 * T::EPI_SPLIT,
+                                      stage_of<T>(sQ, warp));
+            trace_wg(a, kTrSoftmax0, J0 + nk - 1, 7);
             if (nk > 0) {
                 tc_fence_before();
                 mbar_arrive_warp(smem_u32(&aux->bar_odrained));
@@ -1516,12 +1601,16 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         float lf, mf;
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
         if constexpr (PERSIST) {
-            // persistent kernel: O straight from registers to global memory
-            // (the Q tile's shared memory holds the next unit's Q)
+            // persistent kernel: O out through the warp's staging area (the Q
+            // tile's shared memory holds the next unit's Q)
             const int row = w.row0 + t * T::BM + r;
-            uint16_t* orow = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + row) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
-            store_o_rows_direct<T>(lane_base, T::o_col(t), orow, row < a.Sq, nk, inv_l,
-                                   EPI ? 2 * T::EPI_SPLIT : 0, (T::D_COLS + 31) / 32);
+            const int wrow = w.row0 + t * T::BM + (warp & 3) * 32;   // the warp's first row
+            uint16_t* obase = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + wrow) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
+            trace_wg(a, kTrCorr, J0 + w.n_max, 5);
+            store_o_rows_staged<T, 2>(lane_base, T::o_col(t), obase, T::D_COLS * T::DV_SPLIT,
+                                      a.Sq - wrow, nk, inv_l, EPI ? 2 * T::EPI_SPLIT : 0,
+                                      (T::D_COLS + 31) / 32, stage_of<T>(sQ, warp));
+            trace_wg(a, kTrCorr, J0 + w.n_max, 6);
             if (nk > 0) {
                 tc_fence_before();
                 mbar_arrive_warp(smem_u32(&aux->bar_odrained));
