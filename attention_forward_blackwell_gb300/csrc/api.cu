@@ -106,6 +106,22 @@ bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map {d, rows, planes} with a {32, 32, 1} box and 64-byte swizzle
+// (16-byte chunks of each 64-byte row XOR-ed with bits 1-2 of the row): the
+// persistent head_dim-256 kernel's O stores from 2 KB per-warp staging areas.
+bool encode_map32_strided(CUtensorMap* m, const void* base, int d, long long rows,
+                          long long planes, unsigned long long row_stride,
+                          unsigned long long plane_stride) {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
+    const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)plane_stride};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 4-D bf16 map {64 columns, rows, d / 64 chunks, planes} (chunk stride 128
 // bytes) with a {64, 128, 2, 1} box: one copy brings two 64-column chunks of
 // a 128-row tile, written to shared memory as [chunk][row][64 columns] with
@@ -305,7 +321,10 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
             return FA_ERR_INVALID_ARG;
     } else if (!prefill_load_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq, row_bytes,
                                  row_bytes * sq) ||
-               !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq)) {
+               !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq) ||
+               (head_dim == 256 &&
+                !encode_map32_strided(&p.tm_o32, o, head_dim, sq, (long long)batch * hq,
+                                      row_bytes, row_bytes * sq))) {
         return FA_ERR_INVALID_ARG;
     }
     if (block_table) {

@@ -81,6 +81,7 @@ enum TraceRole { kTrMma = 0, kTrSoftmax0 = 1, kTrSoftmax1 = 2, kTrCorr = 3, kTrL
 
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;   // 3-D maps {d, S, B*H}, box {64, 128, 1}
+    CUtensorMap tm_o32;                   // dense head_dim 256: O, box {32, 32, 1}, 64-byte swizzle
     PrefillArgs args;
     int n_tail;                 // split units
     int head_dim;

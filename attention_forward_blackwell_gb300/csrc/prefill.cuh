@@ -1076,11 +1076,18 @@ __device__ __forceinline__ uint32_t stage_of(uint32_t sQ, int warp) {
 // most) and each store instruction writes 8 rows x 64 contiguous bytes (4
 // lanes per row) instead of 32 scattered 16-byte pieces.  obase: the warp's
 // first row at its first column; rows past nvalid are not written.
+//
+// With a 32 x 32 O map (tm_o32 non-null: box {32 columns, 32 rows, 1}, 64-byte
+// swizzle, whose layout is exactly this staging layout) one lane stores each
+// group with a TMA store instead, at (ox + 32 c, oy, oz); the staging area is
+// reused once the previous store has read it.
 template <class T, int NG>
 __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t o_col,
                                                     uint16_t* obase, size_t row_stride,
                                                     int nvalid, int nk, float inv_l,
-                                                    int c_begin, int c_end, uint32_t stage) {
+                                                    int c_begin, int c_end, uint32_t stage,
+                                                    const CUtensorMap* tm_o32 = nullptr,
+                                                    int ox = 0, int oy = 0, int oz = 0) {
     const int lane = threadIdx.x & 31;
 #pragma unroll 1
     for (int cb = c_begin; cb < c_end; cb += NG) {
@@ -1100,6 +1107,10 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
         for (int g = 0; g < NG; ++g) {
             const int c32 = cb + g;
             if (c32 >= c_end) break;
+            if (tm_o32 != nullptr) {   // the previous store must have read the area
+                if (lane == 0) bulk_wait_group_read_0();
+                __syncwarp();
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 uint32_t pk[4];
@@ -1111,6 +1122,15 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[0]),
                              "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                              : "memory");
+            }
+            if (tm_o32 != nullptr) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(tm_o32, stage, ox + c32 * 32, oy, oz);
+                    bulk_commit_group();
+                }
+                continue;
             }
             __syncwarp();
 #pragma unroll
@@ -1195,7 +1215,8 @@ __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const Pref
             trace_wg(a, kTrSoftmax0, J0 + nk - 1, 6);
             store_o_rows_staged<T, 4>(lane_base, T::o_col(t), obase, T::D_COLS * T::DV_SPLIT,
                                       a.Sq - wrow, nk, inv_l, 0, 2 * T::EPI_SPLIT,
-                                      stage_of<T>(sQ, warp));
+                                      stage_of<T>(sQ, warp), tm_o, w.dv0, wrow,
+                                      w.b * a.Hq + w.h);
             trace_wg(a, kTrSoftmax0, J0 + nk - 1, 7);
             if (nk > 0) {
                 tc_fence_before();
@@ -1609,7 +1630,8 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
             trace_wg(a, kTrCorr, J0 + w.n_max, 5);
             store_o_rows_staged<T, 2>(lane_base, T::o_col(t), obase, T::D_COLS * T::DV_SPLIT,
                                       a.Sq - wrow, nk, inv_l, EPI ? 2 * T::EPI_SPLIT : 0,
-                                      (T::D_COLS + 31) / 32, stage_of<T>(sQ, warp));
+                                      (T::D_COLS + 31) / 32, stage_of<T>(sQ, warp), tm_o,
+                                      w.dv0, wrow, w.b * a.Hq + w.h);
             trace_wg(a, kTrCorr, J0 + w.n_max, 6);
             if (nk > 0) {
                 tc_fence_before();
@@ -2070,6 +2092,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             J0 += w.n_max;
             ++kq;
         }
+        if ((threadIdx.x & 31) == 0) bulk_wait_group_read_0();
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
         int J0 = 0, kq = 0;
@@ -2086,6 +2109,8 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             J0 += w.n_max;
             ++kq;
         }
+        // the epilogue's O stores must have read the staging area before exit
+        if ((threadIdx.x & 31) == 0) bulk_wait_group_read_0();
     } else {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::OTHER>();
         if (warp == T::MMA_WARP)
@@ -2129,7 +2154,8 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_TOTAL);
             if (e != cudaSuccess) return e;
             const unsigned grid = (unsigned)min(p.args.n_full, p.num_sms);
-            kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o,
+            // (the persistent kernel stores O through its 32 x 32 map)
+            kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o32,
                                                               p.args);
             return cudaGetLastError();
         }
