@@ -158,10 +158,9 @@ struct PrefillTraits {
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
-    // head_dim 256 (persistent kernel): a 2 KB O staging area for
-    // each of the softmax and correction warps (epilogue stores, see
-    // store_o_rows_staged)
-    static constexpr int SMEM_STAGE = (D == 256) ? 8 * 2048 : 0;
+    // head_dim 256 (persistent kernel): a 2 KB O staging area for each of
+    // the correction warps (epilogue stores, see store_o_rows_staged)
+    static constexpr int SMEM_STAGE = (D == 256) ? 4 * 2048 : 0;
     static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX + SMEM_STAGE;
     static_assert(DV_SPLIT == 1 ? VPIECES == PIECES : NQ == 1,
                   "split output columns only with one Q tile per CTA");
@@ -1061,11 +1060,11 @@ __device__ __forceinline__ void store_o_rows_direct(uint32_t lane_base, uint32_t
     }
 }
 
-// The 2 KB O staging area of warp `warp` (softmax and correction warps
-// 0..7 of a one-tile kernel), after the barrier block.
+// The 2 KB O staging area of warp `warp` of a warpgroup (its index within
+// the group), after the barrier block.
 template <class T>
 __device__ __forceinline__ uint32_t stage_of(uint32_t sQ, int warp) {
-    return sQ + T::SMEM_Q + T::SMEM_RING + T::SMEM_AUX + (uint32_t)(warp & 7) * 2048u;
+    return sQ + T::SMEM_Q + T::SMEM_RING + T::SMEM_AUX + (uint32_t)(warp & 3) * 2048u;
 }
 
 // Writes 32-column groups [c_begin, c_end) of the calling warp's 32 O rows
@@ -1187,7 +1186,7 @@ __host__ __device__ constexpr bool epi_split() {
 // The softmax warpgroup's part of tile t's epilogue (dense launches of
 // whole units): O chunks [0, EPI_SPLIT) staged and stored by this
 // warpgroup once the last value MMA of the tile has completed.
-template <class T, bool VARLEN, bool ENABLED, bool PERSIST>
+template <class T, bool VARLEN, bool ENABLED>
 __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const PrefillArgs& a,
                                       const PrefillWork& w, PrefillAux<T>* aux, uint32_t tmem,
                                       uint32_t sQ, float l, float m, const WaitCtx& wc, int J0) {
@@ -1207,23 +1206,6 @@ __device__ void softmax_epilogue_part(int t, const CUtensorMap* tm_o, const Pref
         }
         float lf, mf;
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
-        if constexpr (PERSIST) {
-            // persistent kernel: the Q tile's shared memory already holds the
-            // next unit's Q, so O goes out through the warp's staging area
-            const int wrow = w.row0 + t * T::BM + (warp & 3) * 32;   // the warp's first row
-            uint16_t* obase = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + wrow) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
-            trace_wg(a, kTrSoftmax0, J0 + nk - 1, 6);
-            store_o_rows_staged<T, 4>(lane_base, T::o_col(t), obase, T::D_COLS * T::DV_SPLIT,
-                                      a.Sq - wrow, nk, inv_l, 0, 2 * T::EPI_SPLIT,
-                                      stage_of<T>(sQ, warp), tm_o, w.dv0, wrow,
-                                      w.b * a.Hq + w.h);
-            trace_wg(a, kTrSoftmax0, J0 + nk - 1, 7);
-            if (nk > 0) {
-                tc_fence_before();
-                mbar_arrive_warp(smem_u32(&aux->bar_odrained));
-            }
-            return;
-        }
         const uint32_t stage = sQ + t * T::QTILE;
         stage_o_rows<T>(lane_base, T::o_col(t), stage, r, nk, inv_l, 0, 2 * T::EPI_SPLIT);
         fence_proxy_async_smem();
@@ -1388,7 +1370,8 @@ __device__ void prefill_softmax_role(int t, const CUtensorMap* tm_o, const Prefi
         aux->mb_l[t][r] = l_run;
         aux->mb_m[t][r] = m_run;
         mbar_arrive_warp(smem_u32(&aux->bar_fin[t]));
-        softmax_epilogue_part<T, VARLEN, epi_split<T, CAUSAL || WINDOW, VARLEN>(), PERSIST>(
+        // (the persistent kernel's correction warpgroup drains all of O)
+        softmax_epilogue_part<T, VARLEN, epi_split<T, CAUSAL || WINDOW, VARLEN>() && !PERSIST>(
             t, tm_o, a, w, aux, tmem, sQ, l_run, m_run, wc, J0);
     }
 }
@@ -1814,9 +1797,11 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
 // running one.  What changes at a unit boundary:
 //   * the producer loads the next unit's Q once the unit's last score MMA
 //     has completed (bar_qfree), not once the unit is over;
-//   * O leaves tensor memory straight to global memory (no staging in the
-//     Q tile's space, which then already holds the next unit's Q), half per
-//     warpgroup, and both warpgroups arrive on bar_odrained when done;
+//   * the correction warpgroup drains O to global memory through a 2 KB
+//     staging area per warp and TMA stores (not through the Q tile's space,
+//     which then already holds the next unit's Q) and arrives on
+//     bar_odrained when done, while the softmax warpgroup goes on with the
+//     next unit's scores;
 //   * the first value MMA of the next unit, which overwrites O, waits for
 //     bar_odrained; so does the softmax before it posts the next unit's
 //     final statistics (their mailbox is read by the correction warpgroup
@@ -2029,8 +2014,10 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     static_assert(T::NQ == 1 && T::DV_SPLIT == 1 && T::CONSUME_ORDER,
                   "persistent kernel: one Q tile, whole output columns, ring in consumption order");
     static_assert(sizeof(PrefillAux<T>) <= T::SMEM_AUX, "auxiliary shared block too large");
-    constexpr bool EPI = epi_split<T, CAUSAL || WINDOW, false>();
-    static_assert(EPI, "persistent kernel: both warpgroups write O");
+    // the correction warpgroup drains all of O: the softmax warpgroup goes
+    // straight on to the next unit's first scores (measured: +0.8 % against
+    // the drain split between the two warpgroups)
+    constexpr bool EPI = false;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t sQ = (raw + 1023u) & ~1023u;
@@ -2059,7 +2046,7 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
         mbar_init(smem_u32(&aux->bar_tail), 1);
         mbar_init(smem_u32(&aux->bar_split_a), 4);
         mbar_init(smem_u32(&aux->bar_qfree), 1);
-        mbar_init(smem_u32(&aux->bar_odrained), 8);   // 4 softmax + 4 correction warps
+        mbar_init(smem_u32(&aux->bar_odrained), 4);   // the 4 correction warps
         aux->abort_flag = 0;
         aux->merge_last = 0;
         mbar_fence_init();
@@ -2092,7 +2079,6 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
             J0 += w.n_max;
             ++kq;
         }
-        if ((threadIdx.x & 31) == 0) bulk_wait_group_read_0();
     } else if (wg == T::CORR_WG) {
         setmaxnreg_dec<T::template Regs<CAUSAL || WINDOW>::CORR>();
         int J0 = 0, kq = 0;
