@@ -158,9 +158,11 @@ struct PrefillTraits {
     static constexpr int SMEM_Q = NQ * QTILE;
     static constexpr int SMEM_RING = NSLOT * SLOT;
     static constexpr int SMEM_AUX = 8192;   // barriers + mailboxes (checked below)
-    // head_dim 256 (persistent kernel): a 2 KB O staging area for each of
-    // the correction warps (epilogue stores, see store_o_rows_staged)
-    static constexpr int SMEM_STAGE = (D == 256) ? 4 * 2048 : 0;
+    // head_dim 256 (persistent kernel): STAGE_BUFS 2 KB O staging buffers
+    // for each of the correction warps (epilogue stores, see
+    // store_o_rows_staged)
+    static constexpr int STAGE_BUFS = 3;
+    static constexpr int SMEM_STAGE = (D == 256) ? 4 * STAGE_BUFS * 2048 : 0;
     static constexpr int SMEM_TOTAL = 1024 + SMEM_Q + SMEM_RING + SMEM_AUX + SMEM_STAGE;
     static_assert(DV_SPLIT == 1 ? VPIECES == PIECES : NQ == 1,
                   "split output columns only with one Q tile per CTA");
@@ -1060,11 +1062,12 @@ __device__ __forceinline__ void store_o_rows_direct(uint32_t lane_base, uint32_t
     }
 }
 
-// The 2 KB O staging area of warp `warp` of a warpgroup (its index within
-// the group), after the barrier block.
+// The O staging buffers (STAGE_BUFS x 2 KB) of warp `warp` of a warpgroup
+// (its index within the group), after the barrier block.
 template <class T>
 __device__ __forceinline__ uint32_t stage_of(uint32_t sQ, int warp) {
-    return sQ + T::SMEM_Q + T::SMEM_RING + T::SMEM_AUX + (uint32_t)(warp & 3) * 2048u;
+    return sQ + T::SMEM_Q + T::SMEM_RING + T::SMEM_AUX +
+           (uint32_t)(warp & 3) * (uint32_t)(T::STAGE_BUFS * 2048);
 }
 
 // Writes 32-column groups [c_begin, c_end) of the calling warp's 32 O rows
@@ -1078,8 +1081,9 @@ __device__ __forceinline__ uint32_t stage_of(uint32_t sQ, int warp) {
 //
 // With a 32 x 32 O map (tm_o32 non-null: box {32 columns, 32 rows, 1}, 64-byte
 // swizzle, whose layout is exactly this staging layout) one lane stores each
-// group with a TMA store instead, at (ox + 32 c, oy, oz); the staging area is
-// reused once the previous store has read it.
+// group with a TMA store instead, at (ox + 32 c, oy, oz), rotating over
+// STAGE_BUFS staging buffers: a buffer is rewritten once the store that last
+// used it has read it.
 template <class T, int NG>
 __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t o_col,
                                                     uint16_t* obase, size_t row_stride,
@@ -1088,6 +1092,12 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
                                                     const CUtensorMap* tm_o32 = nullptr,
                                                     int ox = 0, int oy = 0, int oz = 0) {
     const int lane = threadIdx.x & 31;
+    constexpr int NB = T::STAGE_BUFS > 0 ? T::STAGE_BUFS : 1;
+    int nst = 0;   // TMA stores issued by this call
+    if (tm_o32 != nullptr) {   // an earlier call's stores must have read the buffers
+        if (lane == 0) bulk_wait_group_read_0();
+        __syncwarp();
+    }
 #pragma unroll 1
     for (int cb = c_begin; cb < c_end; cb += NG) {
         uint32_t v[NG][32];
@@ -1106,8 +1116,9 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
         for (int g = 0; g < NG; ++g) {
             const int c32 = cb + g;
             if (c32 >= c_end) break;
-            if (tm_o32 != nullptr) {   // the previous store must have read the area
-                if (lane == 0) bulk_wait_group_read_0();
+            const uint32_t buf = (tm_o32 != nullptr) ? stage + (uint32_t)(nst % NB) * 2048u : stage;
+            if (tm_o32 != nullptr && nst >= NB) {   // the store that last used buf has read it
+                if (lane == 0) bulk_wait_group_read<NB - 1>();
                 __syncwarp();
             }
 #pragma unroll
@@ -1117,7 +1128,7 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
                 for (int e = 0; e < 4; ++e)
                     pk[e] = pack_bf16x2(__uint_as_float(v[g][i * 8 + 2 * e]) * inv_l,
                                         __uint_as_float(v[g][i * 8 + 2 * e + 1]) * inv_l);
-                const uint32_t dst = stage + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+                const uint32_t dst = buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
                 asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(pk[0]),
                              "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
                              : "memory");
@@ -1126,9 +1137,10 @@ __device__ __forceinline__ void store_o_rows_staged(uint32_t lane_base, uint32_t
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(tm_o32, stage, ox + c32 * 32, oy, oz);
+                    tma_store_3d(tm_o32, buf, ox + c32 * 32, oy, oz);
                     bulk_commit_group();
                 }
+                ++nst;
                 continue;
             }
             __syncwarp();

@@ -155,6 +155,11 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
 __device__ __forceinline__ void bulk_wait_group_read_0() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
+// Same, allowing the N most recent groups to be still reading.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 
 // 3-D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, int x, int y,
