@@ -62,8 +62,8 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("adea8be56ed277df78db15a1c82f1867c4184c9dda274217e10e3676350aba47",
-                "long_prefill_b1_h16_s8192_d128", 120432128),
+    "prefill": ("f2529a758ed2077c03e11cc64624d75741750dd5aeecd6fcd4c8ae0b4e73a0e8",
+                "long_prefill_b1_h16_s8192_d128", 120465152),
     # captured at batch 16 (463.35 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
     "decode": ("e51ed49de5a09e0690ddbd22b2e0aee632ee78e4c8991fd3922b1612478162ee",
