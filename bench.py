@@ -64,10 +64,10 @@ CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
     "prefill": ("f2529a758ed2077c03e11cc64624d75741750dd5aeecd6fcd4c8ae0b4e73a0e8",
                 "long_prefill_b1_h16_s8192_d128", 120465152),
-    # captured at batch 16 (463.35 MB, 1.016 x its algorithmic bytes) and
+    # captured at batch 16 (463.46 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
-    "decode": ("e51ed49de5a09e0690ddbd22b2e0aee632ee78e4c8991fd3922b1612478162ee",
-               "decode_gqa_b64_hq64_hkv8_d128", 2203956415),
+    "decode": ("3bb5ba0dff407b1f840b99a70421a37d3691925d34c0806be2ba6dbc45d87e0a",
+               "decode_gqa_b64_hq64_hkv8_d128", 2204477584),
 }
 
 
