@@ -1617,8 +1617,9 @@ __device__ void prefill_correction_role(const CUtensorMap* tm_o, const PrefillAr
         float lf, mf;
         const float inv_l = final_scale(a, w.h, l, m, lf, mf);
         if constexpr (PERSIST) {
-            // persistent kernel: O out through the warp's staging area (the Q
-            // tile's shared memory holds the next unit's Q)
+            // persistent kernel: all of O, through the warp's staging
+            // buffers and TMA stores (the Q tile's shared memory holds the
+            // next unit's Q; the softmax warpgroup has gone on to that unit)
             const int row = w.row0 + t * T::BM + r;
             const int wrow = w.row0 + t * T::BM + (warp & 3) * 32;   // the warp's first row
             uint16_t* obase = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + wrow) * (T::D_COLS * T::DV_SPLIT) + w.dv0;
