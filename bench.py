@@ -62,8 +62,8 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("f2529a758ed2077c03e11cc64624d75741750dd5aeecd6fcd4c8ae0b4e73a0e8",
-                "long_prefill_b1_h16_s8192_d128", 120465152),
+    "prefill": ("b697bb25c6c765e85f63777b37de654b81357e5515d10e0e4e264d102da83bb7",
+                "long_prefill_b1_h16_s8192_d128", 119126784),
     # captured at batch 16 (463.46 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
     "decode": ("3bb5ba0dff407b1f840b99a70421a37d3691925d34c0806be2ba6dbc45d87e0a",
