@@ -78,7 +78,11 @@ typedef enum fa_status {
  * section E steps 3-8).  One CTA per query block (two at head_dim 512, each
  * computing the scores over all 512 dimensions -- the head dimension's
  * sub-tiles summed before the softmax, "STAGE_D.md" hd=512 -- and one
- * 256-column half of O; LSE is stored by the first); for non-causal problems
+ * 256-column half of O; LSE is stored by the first).  At head_dim 256, when
+ * no query block is split and the sequences are not packed, one persistent
+ * CTA per SM processes the query blocks in turn instead (heaviest first over
+ * the SMs, keeping its pipeline state from one block to the next and
+ * storing each block's O while the next one starts).  For non-causal problems
  * the query blocks of the last, partial wave are split along the key axis
  * over several CTAs and merged on the device (see fa_debug_prefill_plan),
  * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
@@ -340,7 +344,9 @@ fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t str
  * SM clock stamps at its pipeline events: role r (0 MMA issue, 1 and 2
  * softmax of query tile 0 and 1, 3 correction/epilogue, 4 TMA producer),
  * event e of key/value iteration j at buf[r * 4096 + j * 16 + e], for the
- * CTA's first work item.  Unused slots are left untouched.  buf = NULL
+ * CTA's first work item (the persistent head_dim-256 kernel: j counts the
+ * key blocks of all its work items in turn).  Unused slots are left
+ * untouched.  buf = NULL
  * switches tracing off.  The stamps are compiled in only when the library is
  * built with FA_PREFILL_TRACE=1 (the Python build reads it from the
  * environment); otherwise a non-NULL buf returns FA_ERR_UNSUPPORTED.
@@ -353,7 +359,8 @@ fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
  * (batch entry, query head, query block of 256 rows for head_dim <= 128, 128
  * for 256 and 512); it visits nk = ceil(sk / 128) key blocks; at head_dim 512
  * it runs as two CTAs and is never split.  The grid's first
- * out[0] CTAs each process a whole unit; the remaining out[1] units (the last
+ * out[0] CTAs each process a whole unit (head_dim 256 with out[1] == 0:
+ * min(out[0], num_sms) persistent CTAs process the out[0] units in turn); the remaining out[1] units (the last
  * partial wave) are each processed by out[2] CTAs, piece i taking key blocks
  * [i nk / out[2], (i + 1) nk / out[2]), and the last piece to finish merges
  * the pieces' partial results.  Returns FA_ERR_INVALID_ARG for sizes that
