@@ -8,6 +8,7 @@ been built, loading it raises.
 """
 from __future__ import annotations
 
+import collections
 import ctypes
 import math
 import os
@@ -48,6 +49,7 @@ SIGNATURES = {
     "fa_debug_prefill_trace": (_I, [_VP, _I]),
     "fa_selftest_exp2_poly": (_I, [_VP, _VP, _I, _VP]),
     "fa_debug_prefill_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _VP]),
+    "fa_debug_prefill_plan_ex": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "fa_version": (_I, []),
 }
 
@@ -368,6 +370,22 @@ def debug_prefill_plan(batch, hq, sq, sk, head_dim, causal, num_sms):
     if st != FA_OK:
         raise FaError(st, "fa_debug_prefill_plan")
     return tuple(out)
+
+
+PrefillPlan = collections.namedtuple(
+    "PrefillPlan", "n_full n_tail split rows_per_unit keys_per_block persistent")
+
+
+def debug_prefill_plan_ex(batch, hq, sq, sk, head_dim, causal, num_sms, *, window=0,
+                          paged=False, packed=False):
+    """The prefill work split of any launch kind (host only, see fa.h)."""
+    out = (ctypes.c_int * 6)()
+    st = lib().fa_debug_prefill_plan_ex(int(batch), int(hq), int(sq), int(sk), int(head_dim),
+                                        int(bool(causal)), int(window), int(bool(paged)),
+                                        int(bool(packed)), int(num_sms), ctypes.addressof(out))
+    if st != FA_OK:
+        raise FaError(st, "fa_debug_prefill_plan_ex")
+    return PrefillPlan(*out[:5], bool(out[5]))
 
 
 def selftest_exp2_poly(x, stream=None):

@@ -90,15 +90,17 @@ unsigned long long next_prefill_epoch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D bf16 map {d, rows, planes} with a {64, 128, 1} box and 128-byte
-// swizzle (rows past `rows` and columns past `d` read as zero).
+// 3-D bf16 map {d, rows, planes} with a {64, box_rows, 1} box (128 rows, or
+// 256 for the K blocks of the 256-key kernels) and 128-byte swizzle (rows
+// past `rows` and columns past `d` read as zero).
 // Strides in bytes: row_stride between rows, plane_stride between planes
 // (contiguous [planes][rows][d] when they are d * 2 and rows * d * 2).
 bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
-                        unsigned long long row_stride, unsigned long long plane_stride) {
+                        unsigned long long row_stride, unsigned long long plane_stride,
+                        unsigned box_rows = 128) {
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
     const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)plane_stride};
-    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t box[3] = {64, box_rows, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -311,6 +313,11 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     }
     PrefillLaunch p{};
     const unsigned long long row_bytes = (unsigned long long)head_dim * 2;
+    // kernel family, unit and block sizes, work split (head_dim 96 / 128,
+    // dense and unmasked: the 256-key kernel)
+    const PrefillShape shape = prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, window,
+                                             block_table != nullptr, vl != nullptr, di->num_sms);
+    const bool wide = shape.wide;
     // Q, O: token-major packed tensors (map {d, tokens, heads}, a token's
     // heads adjacent) or dense [B, Hq, Sq, d]; K, V: paged caches, packed or
     // dense
@@ -322,7 +329,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     } else if (!prefill_load_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq, row_bytes,
                                  row_bytes * sq) ||
                !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq) ||
-               (head_dim == 256 &&
+               ((head_dim == 256 || wide) &&
                 !encode_map32_strided(&p.tm_o32, o, head_dim, sq, (long long)batch * hq,
                                       row_bytes, row_bytes * sq))) {
         return FA_ERR_INVALID_ARG;
@@ -339,8 +346,10 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
             !prefill_load_map(&p.tm_v, v, head_dim, vl->total_k, hkv, row_bytes * hkv, row_bytes,
                               true))
             return FA_ERR_INVALID_ARG;
-    } else if (!prefill_load_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv, row_bytes,
-                                 row_bytes * sk) ||
+    } else if (!(wide ? encode_map_strided(&p.tm_k, k, head_dim, sk, (long long)batch * hkv,
+                                           row_bytes, row_bytes * sk, 256)
+                      : prefill_load_map(&p.tm_k, k, head_dim, sk, (long long)batch * hkv,
+                                         row_bytes, row_bytes * sk)) ||
                !prefill_load_map(&p.tm_v, v, head_dim, sk, (long long)batch * hkv, row_bytes,
                                  row_bytes * sk, true)) {
         return FA_ERR_INVALID_ARG;
@@ -362,8 +371,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     a.Sq = sq;
     a.Sk = sk;
     a.group = hq / hkv;
-    const int rows_per_cta = prefill_rows_per_cta(head_dim);
-    a.num_mblk = (sq + rows_per_cta - 1) / rows_per_cta;
+    a.num_mblk = shape.num_mblk;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_limit_ns = kWaitLimitNs;
     // head_dim 256: the producer of each CTA also prefetches into L2 the Q
@@ -381,22 +389,18 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     p.head_dim = head_dim;
     p.causal = causal ? 1 : 0;
     p.num_sms = di->num_sms;
+    p.wide = wide ? 1 : 0;
     // work split: whole units, then the last partial wave's units in pieces
-    const long long units = (long long)batch * hq * a.num_mblk;
+    const long long units = shape.units;
     if (units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-    a.nk = (sk + 127) / 128;
-    // (a windowed unit has fewer key blocks than nk: it is not split either)
-    // (packed sequences have units of different lengths: not split either)
-    // (head_dim 512 runs two CTAs per unit already: not split either)
-    const PrefillPlan plan =
-        plan_prefill(units, a.nk, p.causal || a.window > 0 || vl != nullptr || head_dim == 512,
-                     di->num_sms);
+    a.nk = shape.nk;
+    const PrefillPlan plan = shape.plan;
     a.n_full = plan.n_full;
     a.split = plan.split;
     p.n_tail = plan.n_tail;
     void* ws = nullptr;
     if (plan.n_tail > 0) {
-        const int nq = rows_per_cta / 128;
+        const int nq = shape.rows_per_unit / 128;
         const size_t pieces = (size_t)plan.n_tail * plan.split;
         const size_t part_o = pieces * nq * head_dim * 128 * sizeof(float);
         const size_t part_ml = pieces * nq * 2 * 128 * sizeof(float);
@@ -621,20 +625,34 @@ fa_status fa_debug_prefill_trace(unsigned long long* buf, int block) {
     return FA_OK;
 }
 
-fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim, int causal,
-                                int num_sms, int* out) {
+fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                   int window, int paged, int packed, int num_sms, int* out) {
     if (!out || batch <= 0 || hq <= 0 || sq <= 0 || sk <= 0 || batch > 65535 || hq > 65535 ||
         num_sms < 1)
         return FA_ERR_INVALID_ARG;
     if (!prefill_head_dim_ok(head_dim)) return FA_ERR_INVALID_ARG;
-    const int rows = prefill_rows_per_cta(head_dim);
-    const long long units = (long long)batch * hq * ((sq + rows - 1) / rows);
-    if (units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
-    const PrefillPlan p =
-        plan_prefill(units, (sk + 127) / 128, (causal || head_dim == 512) ? 1 : 0, num_sms);
-    out[0] = p.n_full;
-    out[1] = p.n_tail;
-    out[2] = p.split;
+    const PrefillShape sh = prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, window,
+                                          paged != 0, packed != 0, num_sms);
+    if (sh.units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+    out[0] = sh.plan.n_full;
+    out[1] = sh.plan.n_tail;
+    out[2] = sh.plan.split;
+    out[3] = sh.rows_per_unit;
+    out[4] = sh.keys_per_block;
+    out[5] = sh.persistent ? 1 : 0;
+    return FA_OK;
+}
+
+fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                int num_sms, int* out) {
+    if (!out) return FA_ERR_INVALID_ARG;
+    int full[6];
+    const fa_status st =
+        fa_debug_prefill_plan_ex(batch, hq, sq, sk, head_dim, causal, 0, 0, 0, num_sms, full);
+    if (st != FA_OK) return st;
+    out[0] = full[0];
+    out[1] = full[1];
+    out[2] = full[2];
     return FA_OK;
 }
 

@@ -49,7 +49,7 @@ struct PrefillArgs {
     // each later unit is split into `split` pieces of its nk key blocks.
     int n_full;
     int split;
-    int nk;                     // key blocks of a unit, ceil(Sk / 128)
+    int nk;                     // key blocks of a unit, ceil(Sk / keys per block)
     // Scratch of the split units (nullptr when nothing is split): partial O
     // of every piece, [pieces][NQ][d / 4][128][4] fp32, its row max and row
     // sum, [pieces][NQ][2][128] fp32, and one arrival counter per split unit,
@@ -81,14 +81,23 @@ enum TraceRole { kTrMma = 0, kTrSoftmax0 = 1, kTrSoftmax1 = 2, kTrCorr = 3, kTrL
 
 struct PrefillLaunch {
     CUtensorMap tm_q, tm_k, tm_v, tm_o;   // 3-D maps {d, S, B*H}, box {64, 128, 1}
-    CUtensorMap tm_o32;                   // dense head_dim 256: O, box {32, 32, 1}, 64-byte swizzle
+    CUtensorMap tm_o32;                   // persistent kernels: O, box {32, 32, 1}, 64-byte swizzle
     PrefillArgs args;
     int n_tail;                 // split units
     int head_dim;
     int causal;
     int num_sms;                // SMs of the device (CTAs of a persistent launch)
+    int wide;                   // prefill_wide_ok: 256-key score blocks (units of 128 query
+                                // rows, tm_k box {64, 256, 1}, tm_o32 set)
 };
 
+// The 256-key persistent kernel (head_dim 96 and 128) takes dense launches
+// without a mask: no causal mask, no window, contiguous K/V (no block
+// table), no packed sequences.  (Causal launches measured 2-4 % faster on
+// the two-tile kernel: a 256-key block on the diagonal is up to half masked.)
+inline bool prefill_wide_ok(int head_dim, bool causal, int window, bool paged, bool packed) {
+    return (head_dim == 96 || head_dim == 128) && !causal && window <= 0 && !paged && !packed;
+}
 // Query rows of one prefill unit (query block) for a head dimension.
 inline int prefill_rows_per_cta(int head_dim) { return head_dim <= 128 ? 256 : 128; }
 // CTAs per unit: head_dim 512 shares the output columns out over two.
@@ -127,6 +136,41 @@ inline PrefillPlan plan_prefill(long long units, int nk, int causal, int ctas) {
     p.n_tail = (int)tail;
     p.split = (int)k;
     return p;
+}
+
+// How a prefill launch is cut into work: which kernel family runs it, the
+// query rows of a unit, the keys of a score block and the work split.  One
+// function serves the launch and the plan queries, so that they agree.
+struct PrefillShape {
+    bool wide;             // prefill_wide_ok: the 256-key persistent kernel
+    int rows_per_unit;     // query rows of a unit (query block)
+    int keys_per_block;    // keys of a score block
+    int num_mblk;          // units per (batch entry, query head)
+    long long units;
+    int nk;                // key blocks of a unit
+    PrefillPlan plan;
+    bool persistent;       // one CTA per SM walks the unit list
+};
+
+inline PrefillShape prefill_shape(int batch, int hq, int sq, int sk, int head_dim, bool causal,
+                                  int window, bool paged, bool packed, int num_sms) {
+    PrefillShape s;
+    s.wide = prefill_wide_ok(head_dim, causal, window, paged, packed);
+    s.rows_per_unit = s.wide ? 128 : prefill_rows_per_cta(head_dim);
+    s.keys_per_block = s.wide ? 256 : 128;
+    s.num_mblk = (sq + s.rows_per_unit - 1) / s.rows_per_unit;
+    s.units = (long long)batch * hq * s.num_mblk;
+    s.nk = (sk + s.keys_per_block - 1) / s.keys_per_block;
+    // not split: causal units (heaviest first), windowed ones (fewer key
+    // blocks than nk), packed sequences (units of different lengths), head_dim
+    // 512 (two CTAs per unit already), the persistent 256-key kernel
+    s.plan = plan_prefill(s.units, s.nk,
+                          causal || window > 0 || packed || head_dim == 512 || s.wide, num_sms);
+    // head_dim 256 launches of whole units, and the 256-key kernel, run one
+    // persistent CTA per SM
+    s.persistent = s.wide || (head_dim == 256 && !packed && s.plan.n_tail == 0 &&
+                              s.plan.n_full > 0 && num_sms > 0);
+    return s;
 }
 
 cudaError_t launch_prefill_d64(const PrefillLaunch& p, cudaStream_t s);

@@ -222,7 +222,8 @@ struct PrefillAux {
 enum : unsigned int {
     kSiteLoadEmpty = 1, kSiteMmaQ, kSiteMmaK, kSiteMmaV, kSiteMmaP, kSiteLoadTail, kSiteMmaPv,
     kSiteSmS, kSiteSmMbox, kSiteCorrMbox, kSiteCorrPv, kSiteEpiMbox, kSiteEpiPv,
-    kSiteEpiStage, kSiteSplitA, kSiteLoadQfree, kSiteMmaOdrained, kSiteSmOdrained, kSiteSmPv
+    kSiteEpiStage, kSiteSplitA, kSiteLoadQfree, kSiteMmaOdrained, kSiteSmOdrained, kSiteSmPv,
+    kSiteSmXm, kSiteMmaSfree
 };
 
 // Recorded if a piece's arrival could not be counted (never expected: every
@@ -2127,6 +2128,12 @@ __global__ void __launch_bounds__(PrefillTraits<D>::THREADS, 1)
     }
 }
 
+}  // namespace fa
+
+#include "prefill_wide.cuh"
+
+namespace fa {
+
 // Host-side launch of one head-dimension instantiation.
 using PrefillKernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, PrefillArgs);
 
@@ -2155,6 +2162,20 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
             const unsigned grid = (unsigned)min(p.args.n_full, p.num_sms);
             // (the persistent kernel stores O through its 32 x 32 map)
             kern<<<grid, T::THREADS, T::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o32,
+                                                              p.args);
+            return cudaGetLastError();
+        }
+    }
+    if constexpr (D == 96 || D == 128) {
+        // dense, unmasked: 256-key score blocks, one persistent CTA per SM
+        if (p.wide) {
+            using W = WideTraits<D>;
+            const PrefillKernelFn kern = prefill_kernel_wide<D>;
+            cudaError_t e = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W::SMEM_TOTAL);
+            if (e != cudaSuccess) return e;
+            const unsigned grid = (unsigned)min(p.args.n_full, p.num_sms);
+            kern<<<grid, W::THREADS, W::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o32,
                                                               p.args);
             return cudaGetLastError();
         }

@@ -53,6 +53,7 @@ PAGES_FWD_TFLOPS_B1_S8192_H16_D128 = 275.5
 # entries are reported as null.
 KERNEL_SOURCES = {
     "prefill": ["attention_forward_blackwell_gb300/csrc/prefill.cuh",
+                "attention_forward_blackwell_gb300/csrc/prefill_wide.cuh",
                 "attention_forward_blackwell_gb300/csrc/ptx.cuh",
                 "attention_forward_blackwell_gb300/csrc/common.cuh"],
     "decode": ["attention_forward_blackwell_gb300/csrc/decode.cu",
@@ -412,7 +413,8 @@ def run_ours(args, dist):
                    "parallelism": ("one GPU" if dist.world == 1 else
                                    f"(batch, kv head) pairs sharded over {dist.world} ranks")},
         "breakdown": breakdown,
-        "roofline": {"kernel": "prefill_kernel<128, non-causal> (headline launch)",
+        "roofline": {"kernel": "prefill_kernel_wide<128> (persistent, 256-key blocks; "
+                               "headline launch)",
                      "bound": "tensor", "achieved": value,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(value / peaks["bf16_tflops"], 4),

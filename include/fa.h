@@ -82,9 +82,16 @@ typedef enum fa_status {
  * no query block is split and the sequences are not packed, one persistent
  * CTA per SM processes the query blocks in turn instead (heaviest first over
  * the SMs, keeping its pipeline state from one block to the next and
- * storing each block's O while the next one starts).  For non-causal problems
- * the query blocks of the last, partial wave are split along the key axis
- * over several CTAs and merged on the device (see fa_debug_prefill_plan),
+ * storing each block's O while the next one starts).  At head_dim 96 and 128
+ * without a causal mask (also without a window, paged caches or packed
+ * sequences), a persistent kernel with 256-key score blocks and query blocks
+ * of 128 rows runs instead: one N = 256 score MMA per K-step, P in tensor
+ * memory columns of its own, the next block's score MMA issued while the
+ * softmax of this one runs, each row's softmax split over two warpgroups
+ * (128 keys each) that exchange their block maxima.  For the other
+ * non-causal problems the query blocks of the last, partial wave are split
+ * along the key axis over several CTAs and merged on the device (see
+ * fa_debug_prefill_plan_ex),
  * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
  * with cudaFreeAsync on the same stream) of at most SMs * 130 KB (head_dim
  * 128; in proportion for other head dims).
@@ -342,10 +349,11 @@ fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t str
  * values, the following prefill launches make one thread of each role of the
  * CTA with linear index `block` (x + gridDim.x * (y + gridDim.y * z)) record
  * SM clock stamps at its pipeline events: role r (0 MMA issue, 1 and 2
- * softmax of query tile 0 and 1, 3 correction/epilogue, 4 TMA producer),
- * event e of key/value iteration j at buf[r * 4096 + j * 16 + e], for the
- * CTA's first work item (the persistent head_dim-256 kernel: j counts the
- * key blocks of all its work items in turn).  Unused slots are left
+ * softmax of query tile 0 and 1 -- of key half 0 and 1 in the 256-key
+ * kernel --, 3 correction/epilogue, 4 TMA producer), event e of key/value
+ * iteration j at buf[r * 4096 + j * 16 + e], for the CTA's first work item
+ * (the persistent kernels: j counts the key blocks of all its work items in
+ * turn).  Unused slots are left
  * untouched.  buf = NULL
  * switches tracing off.  The stamps are compiled in only when the library is
  * built with FA_PREFILL_TRACE=1 (the Python build reads it from the
@@ -354,18 +362,30 @@ fa_status fa_selftest_exp2_poly(const float *x, float *y, int n, fa_stream_t str
 fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
 
 /*
- * The work split fa_fwd_prefill would use for a problem on a device with
- * `num_sms` SMs, computed on the host (no device needed).  A unit is one
- * (batch entry, query head, query block of 256 rows for head_dim <= 128, 128
- * for 256 and 512); it visits nk = ceil(sk / 128) key blocks; at head_dim 512
- * it runs as two CTAs and is never split.  The grid's first
- * out[0] CTAs each process a whole unit (head_dim 256 with out[1] == 0:
- * min(out[0], num_sms) persistent CTAs process the out[0] units in turn); the remaining out[1] units (the last
- * partial wave) are each processed by out[2] CTAs, piece i taking key blocks
- * [i nk / out[2], (i + 1) nk / out[2]), and the last piece to finish merges
- * the pieces' partial results.  Returns FA_ERR_INVALID_ARG for sizes that
- * fa_fwd_prefill rejects or num_sms < 1.
+ * The work split a prefill launch would use on a device with `num_sms` SMs,
+ * computed on the host (no device needed).  window: as fa_fwd_prefill_ex;
+ * paged: nonzero for fa_fwd_prefill_paged; packed: nonzero for the packed
+ * sequences of fa_fwd_prefill_varlen (sq is then the largest query length).
+ * A unit is one (batch entry, query head, query block of out[3] rows); it
+ * visits nk = ceil(sk / out[4]) key blocks; at head_dim 512 it runs as two
+ * CTAs and is never split.  out[5] == 1: min(out[0], num_sms) persistent
+ * CTAs process the out[0] units in turn (the 256-key kernel of head_dim 96 /
+ * 128, and head_dim 256 when nothing is split).  Otherwise the grid's first
+ * out[0] CTAs each process a whole unit, and the remaining out[1] units (the
+ * last partial wave) are each processed by out[2] CTAs, piece i taking key
+ * blocks [i nk / out[2], (i + 1) nk / out[2]); the last piece to finish
+ * merges the pieces' partial results.  out: int[6]
+ *   out[0] n_full, out[1] n_tail, out[2] split, out[3] query rows of a unit
+ *   (128 or 256), out[4] keys of a score block (128 or 256), out[5]
+ *   persistent.
+ * Returns FA_ERR_INVALID_ARG for sizes that fa_fwd_prefill rejects or
+ * num_sms < 1.
  */
+fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                   int window, int paged, int packed, int num_sms, int *out);
+
+/* fa_debug_prefill_plan_ex of a dense launch without a window (window = 0,
+ * paged = packed = 0), out[0..2] only (out: int[3]). */
 fa_status fa_debug_prefill_plan(int batch, int hq, int sq, int sk, int head_dim, int causal,
                                 int num_sms, int *out);
 

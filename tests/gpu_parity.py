@@ -2,6 +2,7 @@
 the very same seeded inputs and compare element by element."""
 from __future__ import annotations
 
+import math
 import os
 
 import numpy as np
@@ -73,3 +74,27 @@ def check_device_error():
 def free_cuda():
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+
+
+def to_pages(k, v, lens, page_size, seed, spare=3):
+    """Scatter K, V [B, Hkv, Sk, d] into shuffled pages [num_pages, Hkv, P, d].
+    Rows past each length and every unused page hold NaN (never read)."""
+    B, Hkv, Sk, d = k.shape
+    max_pages = math.ceil(Sk / page_size)
+    need = [math.ceil(L / page_size) for L in lens]
+    num_pages = sum(need) + spare
+    perm = np.random.default_rng(seed).permutation(num_pages)
+    kc = torch.full((num_pages, Hkv, page_size, d), float("nan"), device=k.device,
+                    dtype=k.dtype)
+    vc = kc.clone()
+    table = torch.zeros(B, max_pages, dtype=torch.int32)
+    nxt = 0
+    for b in range(B):
+        for i in range(need[b]):
+            pg = int(perm[nxt])
+            nxt += 1
+            table[b, i] = pg
+            lo, hi = i * page_size, min((i + 1) * page_size, lens[b])
+            kc[pg, :, :hi - lo] = k[b, :, lo:hi]
+            vc[pg, :, :hi - lo] = v[b, :, lo:hi]
+    return kc, vc, table.cuda(), num_pages

@@ -101,7 +101,7 @@ def test_prefill_d512_paged_matches_contiguous():
     """Shuffled, NaN-poisoned pages of 128 keys: the oracle, and bit for bit
     the contiguous call on the same keys."""
     from attention_forward_blackwell_gb300 import binding, inputs
-    from test_paged_gpu import to_pages
+    from gpu_parity import to_pages
     B, Hq, Hkv, Sq, Sk = 2, 4, 2, 200, 640
     lengths = [640, 333]
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, D, tag=5200, device="cuda", lengths=lengths)

@@ -48,8 +48,9 @@ PREFILL = [
     (1, 4, 2, 300, 500, 256, True, 129, True, None),
     (1, 4, 2, 300, 500, 256, False, 64, False, None),
     (1, 2, 2, 333, 200, 128, True, 50, True, None),       # Sq > Sk: leading rows see no key
-    (1, 2, 2, 1000, 1000, 128, False, 0, True, None),     # sinks only (split blocks merge them)
-    (1, 1, 1, 16384, 16384, 128, False, 0, True, None),   # sinks through the split-block merge
+    (1, 2, 2, 1000, 1000, 128, False, 0, True, None),     # sinks only (256-key kernel)
+    (1, 2, 1, 1000, 1500, 96, False, 0, True, [1433]),    # sinks only (256-key kernel), d = 96
+    (1, 1, 1, 16384, 16384, 64, False, 0, True, None),    # sinks through the split-block merge
 ]
 
 

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_parity import check_device_error, compare, free_cuda, oracle_for
+from gpu_parity import check_device_error, compare, free_cuda, oracle_for, to_pages
 
 pytestmark = pytest.mark.gpu
 
@@ -19,28 +19,10 @@ def built():
     free_cuda()
 
 
-def to_pages(k, v, lens, page_size, seed, spare=3):
-    """Scatter K, V [B, Hkv, Sk, d] into shuffled pages [num_pages, Hkv, P, d].
-    Rows past each length and every unused page hold NaN (never read)."""
-    B, Hkv, Sk, d = k.shape
-    max_pages = math.ceil(Sk / page_size)
-    need = [math.ceil(L / page_size) for L in lens]
-    num_pages = sum(need) + spare
-    perm = np.random.default_rng(seed).permutation(num_pages)
-    kc = torch.full((num_pages, Hkv, page_size, d), float("nan"), device=k.device,
-                    dtype=k.dtype)
-    vc = kc.clone()
-    table = torch.zeros(B, max_pages, dtype=torch.int32)
-    nxt = 0
-    for b in range(B):
-        for i in range(need[b]):
-            pg = int(perm[nxt])
-            nxt += 1
-            table[b, i] = pg
-            lo, hi = i * page_size, min((i + 1) * page_size, lens[b])
-            kc[pg, :, :hi - lo] = k[b, :, lo:hi]
-            vc[pg, :, :hi - lo] = v[b, :, lo:hi]
-    return kc, vc, table.cuda(), num_pages
+def _wide(B, Hq, Sq, Sk, d, causal):
+    """A contiguous launch of this shape runs the 256-key kernel."""
+    from attention_forward_blackwell_gb300 import binding
+    return binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, causal, 152).keys_per_block == 256
 
 
 PREFILL = [
@@ -67,8 +49,10 @@ def test_prefill_paged(B, Hq, Hkv, Sq, Sk, d, P, causal, lengths):
     check_device_error()
     ro, rl = oracle_for(x, scale, causal)
     compare(o, lse, ro, rl, f"prefill paged P={P}")
-    # the same kernel on contiguous K/V of the same (page-rounded) length
-    if Sk % P == 0:
+    # contiguous K/V of the same (page-rounded) length: the same kernel gives
+    # the same result bit for bit (the 256-key kernel, which takes the
+    # contiguous non-causal head_dim-96/128 launches, is checked on its own)
+    if Sk % P == 0 and not _wide(B, Hq, Sq, Sk, d, causal):
         o2, l2 = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal,
                                  seqlens_k=x.seqlens_k)
         torch.cuda.synchronize()
@@ -81,6 +65,7 @@ SPLIT_PAGED = [
     # least 16 key blocks whose units do not fill a wave, so the plan cuts
     # them into pieces along the key axis (page lookups inside every piece)
     (2, 2, 1, 1024, 2560, 128, 256, [2560, 2300]),
+    (2, 2, 1, 1024, 2560, 96, 256, [2560, 1800]),
     (1, 4, 2, 512, 2048, 256, 128, [2048]),
     (2, 2, 2, 1024, 3072, 64, 512, [3000, 2049]),
 ]
@@ -91,10 +76,11 @@ SPLIT_PAGED = [
 def test_prefill_paged_split_units(B, Hq, Hkv, Sq, Sk, d, P, lengths):
     """Paged caches with the last wave split into pieces and merged on the
     device: every row against the oracle, and bit-equal to the same plan on
-    contiguous K/V."""
+    contiguous K/V where the contiguous launch runs the same kernel (else
+    that one against the oracle too)."""
     from attention_forward_blackwell_gb300 import binding, inputs
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert binding.debug_prefill_plan(B, Hq, Sq, Sk, d, False, n_sms)[2] > 1
+    assert binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, False, n_sms, paged=True).split > 1
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=850 + d, device="cuda", lengths=lengths)
     kc, vc, table, _ = to_pages(x.k, x.v, lengths, P, seed=P + d)
     scale = 1.0 / math.sqrt(d)
@@ -107,7 +93,11 @@ def test_prefill_paged_split_units(B, Hq, Hkv, Sq, Sk, d, P, lengths):
     inputs.poison_beyond_lengths(x.v, x.seqlens_k)
     o2, l2 = binding.prefill(x.q, x.k, x.v, scale=scale, seqlens_k=x.seqlens_k)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    check_device_error()
+    if _wide(B, Hq, Sq, Sk, d, False):
+        compare(o2, l2, ro, rl, f"prefill contiguous (256-key kernel) d={d}")
+    else:
+        assert torch.equal(o, o2) and torch.equal(lse, l2)
     free_cuda()
 
 

@@ -96,7 +96,7 @@ def test_persistent_window_and_sinks():
 
 def test_persistent_paged_matches_contiguous():
     from attention_forward_blackwell_gb300 import binding, inputs
-    from test_paged_gpu import to_pages
+    from gpu_parity import to_pages
     B, Hq, Hkv, Sq, Sk, P = 6, 16, 2, 512, 1024, 256
     lens = [1024, 0, 300, 1024, 129, 777]
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, 256, tag=1760, device="cuda", lengths=lens)

@@ -187,12 +187,12 @@ def test_barrier_protocol_stress(B, Hq, Sq, Sk, d, causal):
 SPLIT = [
     # B, Hq, Hkv, Sq, Sk, d, lengths: non-causal shapes whose query blocks do
     # not fill whole waves of the GPU, so the last wave's blocks are computed
-    # in pieces along the key axis and merged on the device
-    (1, 1, 1, 16384, 16384, 128, None),     # 64 blocks -> 2 pieces each
-    (1, 2, 2, 5000, 7000, 96, None),        # 40 blocks -> 3 pieces each
+    # in pieces along the key axis and merged on the device (head_dim 96 and
+    # 128 split only on paged caches: test_paged_gpu.py)
+    (1, 1, 1, 16384, 16384, 64, None),      # 64 blocks -> 2 pieces each
     (1, 2, 2, 3000, 9000, 256, None),       # 48 blocks -> 3 pieces each
     (3, 1, 1, 2000, 30000, 64, [30000, 0, 17]),   # 24 blocks -> 6 pieces; empty pieces
-    (2, 16, 4, 4096, 4096, 128, None),      # the bench shape with GQA: 56 tail blocks
+    (2, 16, 4, 4096, 4096, 64, None),       # GQA: 56 tail blocks -> 2 pieces each
 ]
 
 
@@ -202,7 +202,8 @@ def test_split_units_sampled_rows(B, Hq, Hkv, Sq, Sk, d, lengths):
     """Query blocks computed in pieces by several CTAs and merged by the last
     piece to finish: sampled rows (tile edges of a few heads plus random rows)
     against the oracle, finiteness of every output row that sees a key."""
-    from attention_forward_blackwell_gb300 import inputs
+    from attention_forward_blackwell_gb300 import binding, inputs
+    assert binding.debug_prefill_plan(B, Hq, Sq, Sk, d, False, 152)[2] > 1   # split
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=500 + Sq % 97, device="cuda",
                            lengths=lengths)
     if lengths is not None:
@@ -226,8 +227,9 @@ def test_split_units_sampled_rows(B, Hq, Hkv, Sq, Sk, d, lengths):
 
 def test_split_units_are_deterministic():
     """The merge of split units does not depend on which piece arrives last."""
-    from attention_forward_blackwell_gb300 import inputs
-    x = inputs.make_inputs(1, 1, 1, 16384, 16384, 128, tag=503, device="cuda")
+    from attention_forward_blackwell_gb300 import binding, inputs
+    assert binding.debug_prefill_plan(1, 1, 16384, 16384, 64, False, 152)[2] > 1   # split
+    x = inputs.make_inputs(1, 1, 1, 16384, 16384, 64, tag=503, device="cuda")
     o1, l1 = _run(x, 0.088, False)
     for _ in range(5):
         o2, l2 = _run(x, 0.088, False)
@@ -239,8 +241,8 @@ def test_split_units_replay_in_a_cuda_graph():
     captured in a CUDA graph and replayed: every replay equals the eager
     result bit for bit (the last piece resets its counter)."""
     from attention_forward_blackwell_gb300 import binding, inputs
-    x = inputs.make_inputs(1, 2, 2, 4096, 4096, 128, tag=990, device="cuda")
-    assert binding.debug_prefill_plan(1, 2, 4096, 4096, 128, 0, 152)[2] > 1   # split
+    x = inputs.make_inputs(1, 2, 2, 4096, 4096, 64, tag=990, device="cuda")
+    assert binding.debug_prefill_plan(1, 2, 4096, 4096, 64, 0, 152)[2] > 1   # split
     o_ref, l_ref = binding.prefill(x.q, x.k, x.v)
     o = torch.empty_like(x.q)
     lse = torch.empty(1, 2, 4096, device="cuda")
@@ -283,15 +285,15 @@ def test_wide_grids(B, Hq, Hkv, S, d, causal):
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_long_context_128k_sampled(causal):
-    """One head over 131,072 keys (up to 1,024 key blocks per unit; the
-    non-causal launch computes the 56 units of its last partial wave in two
-    pieces each, the causal one runs units of 2 to 1,024 blocks heaviest
-    first): finiteness everywhere, sampled rows (tile edges at the start,
-    middle and end plus random rows) against the oracle."""
+    """One head over 131,072 keys (the non-causal launch runs the persistent
+    256-key kernel over 1,024 units of 512 key blocks; the causal one runs
+    units of 2 to 1,024 blocks of 128 keys heaviest first): finiteness
+    everywhere, sampled rows (tile edges at the start, middle and end plus
+    random rows) against the oracle."""
     from attention_forward_blackwell_gb300 import binding, inputs
     S, d = 131072, 128
     if not causal:
-        assert binding.debug_prefill_plan(1, 1, S, S, d, 0, 152) == (456, 56, 2)
+        assert binding.debug_prefill_plan_ex(1, 1, S, S, d, 0, 152) == (1024, 0, 1, 128, 256, True)
     x = inputs.make_inputs(1, 1, 1, S, S, d, tag=1300, device="cuda")
     scale = 1.0 / math.sqrt(d)
     o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal)

@@ -1,5 +1,6 @@
-"""Host logic of the prefill work split: which query blocks run whole and
-which are split along the key axis (no GPU needed)."""
+"""Host logic of the prefill work split: which kernel family runs a launch,
+the sizes of its units and key blocks, and which query blocks run whole or
+are split along the key axis (no GPU needed)."""
 import math
 
 import pytest
@@ -8,46 +9,89 @@ from attention_forward_blackwell_gb300 import binding
 
 SHAPES = [
     # batch, hq, sq, sk, head_dim, causal
-    (2, 16, 4096, 4096, 128, False),   # the bench: 512 blocks, 56 in the last wave
+    (2, 16, 4096, 4096, 128, False),   # the bench workloads
     (2, 16, 4096, 4096, 128, True),
     (1, 16, 8192, 8192, 128, False),
     (2, 16, 4096, 4096, 96, False),
     (4, 32, 2048, 2048, 256, True),
+    (4, 32, 2048, 2048, 64, False),
     (1, 1, 16384, 16384, 128, False),  # fewer blocks than SMs
     (1, 2, 5000, 7000, 96, False),
     (1, 2, 3000, 9000, 256, False),
     (3, 1, 2000, 30000, 64, False),
     (1, 1, 128, 128, 64, False),       # one block of one key tile
-    (19, 8, 4096, 4096, 128, False),   # 304 blocks: whole waves only
-    (1, 1, 300, 1000, 128, False),     # key tiles too few to split
+    (19, 8, 4096, 4096, 128, False),
+    (19, 8, 4096, 4096, 64, False),    # 304 blocks: whole waves only
+    (1, 1, 300, 1000, 128, False),
+    (2, 8, 4096, 4096, 512, False),
+]
+KINDS = [
+    # window, paged, packed
+    (0, False, False),
+    (0, True, False),
+    (0, False, True),
+    (1024, False, False),
 ]
 
 
+def _wide(d, causal, window, paged, packed):
+    """The 256-key persistent kernel: head_dim 96 / 128, dense, unmasked."""
+    return d in (96, 128) and not causal and window <= 0 and not paged and not packed
+
+
+@pytest.mark.parametrize("kind", KINDS, ids=[str(k) for k in KINDS])
 @pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
 @pytest.mark.parametrize("sms", [152, 148, 7])
-def test_plan_invariants(shape, sms):
+def test_plan_invariants(shape, kind, sms):
     batch, hq, sq, sk, d, causal = shape
-    n_full, n_tail, split = binding.debug_prefill_plan(batch, hq, sq, sk, d, causal, sms)
-    rows = 256 if d <= 128 else 128
-    units = batch * hq * math.ceil(sq / rows)
-    nk = math.ceil(sk / 128)
-    assert n_full + n_tail == units
-    if split == 1:
-        assert n_tail == 0
+    window, paged, packed = kind
+    p = binding.debug_prefill_plan_ex(batch, hq, sq, sk, d, causal, sms, window=window,
+                                      paged=paged, packed=packed)
+    wide = _wide(d, causal, window, paged, packed)
+    assert p.rows_per_unit == (128 if wide or d >= 256 else 256)
+    assert p.keys_per_block == (256 if wide else 128)
+    units = batch * hq * math.ceil(sq / p.rows_per_unit)
+    nk = math.ceil(sk / p.keys_per_block)
+    assert p.n_full + p.n_tail == units
+    if wide:
+        # persistent, whole units
+        assert p.persistent and (p.n_full, p.n_tail, p.split) == (units, 0, 1)
+        return
+    assert p.persistent == (d == 256 and not packed and p.n_tail == 0 and p.n_full > 0)
+    if p.split == 1:
+        assert p.n_tail == 0
     else:
-        assert not causal                          # causal blocks are never split
-        assert n_tail == units % sms and n_tail > 0
-        assert n_full % sms == 0                   # whole blocks fill whole waves
-        assert n_tail * split <= sms               # every piece runs in one wave
-        assert nk // split >= 8                    # at least 8 key tiles per piece
-        assert 2 <= split <= 8
+        # causal, windowed, packed and head_dim-512 units are never split
+        assert not causal and window <= 0 and not packed and d != 512
+        assert p.n_tail == units % sms and p.n_tail > 0
+        assert p.n_full % sms == 0                     # whole blocks fill whole waves
+        assert p.n_tail * p.split <= sms               # every piece runs in one wave
+        assert nk // p.split >= 8                      # at least 8 key tiles per piece
+        assert 2 <= p.split <= 8
         # the largest such split
-        assert split == 8 or n_tail * (split + 1) > sms or nk // (split + 1) < 8
+        assert p.split == 8 or p.n_tail * (p.split + 1) > sms or nk // (p.split + 1) < 8
 
 
-def test_plan_of_the_bench_workload():
-    assert binding.debug_prefill_plan(2, 16, 4096, 4096, 128, False, 152) == (456, 56, 2)
-    assert binding.debug_prefill_plan(2, 16, 4096, 4096, 128, True, 152) == (512, 0, 1)
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_dense_plan_is_the_extended_one(shape):
+    """fa_debug_prefill_plan is the dense, unwindowed case of the extended query."""
+    batch, hq, sq, sk, d, causal = shape
+    assert binding.debug_prefill_plan(batch, hq, sq, sk, d, causal, 152) == \
+        tuple(binding.debug_prefill_plan_ex(batch, hq, sq, sk, d, causal, 152)[:3])
+
+
+def test_plan_of_the_bench_workloads():
+    plan = binding.debug_prefill_plan_ex
+    # non-causal head_dim 128: 256-key kernel, 1024 units of 128 rows, persistent
+    assert plan(2, 16, 4096, 4096, 128, False, 152) == (1024, 0, 1, 128, 256, True)
+    assert plan(1, 16, 8192, 8192, 128, False, 152) == (1024, 0, 1, 128, 256, True)
+    # causal: two-tile kernel, heaviest first, one CTA per unit
+    assert plan(2, 16, 4096, 4096, 128, True, 152) == (512, 0, 1, 256, 128, False)
+    # the same non-causal problem on paged caches: the last wave split in two
+    assert plan(2, 16, 4096, 4096, 128, False, 152, paged=True) == (456, 56, 2, 256, 128, False)
+    # causal GQA head_dim 256: persistent over 2048 units
+    assert plan(4, 32, 2048, 2048, 256, True, 152) == (2048, 0, 1, 128, 128, True)
+    assert binding.debug_prefill_plan(2, 16, 4096, 4096, 128, False, 152) == (1024, 0, 1)
 
 
 def test_plan_rejects_bad_sizes():
@@ -55,3 +99,5 @@ def test_plan_rejects_bad_sizes():
         binding.debug_prefill_plan(1, 1, 128, 128, 80, False, 152)
     with pytest.raises(binding.FaError):
         binding.debug_prefill_plan(1, 1, 128, 128, 128, False, 0)
+    with pytest.raises(binding.FaError):
+        binding.debug_prefill_plan_ex(1, 1, 128, 128, 128, False, 0, paged=True)

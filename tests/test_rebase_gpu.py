@@ -132,9 +132,18 @@ def lazy_rebases(t, groups):
     return count
 
 
-def prefill_blocks(Sk, kb=0, ke=None):
-    ke = (Sk + 127) // 128 if ke is None else ke
-    return [np.arange(j * 128, min((j + 1) * 128, Sk)) for j in range(kb, ke)]
+def prefill_blocks(Sk, kb=0, ke=None, bs=128):
+    """Key blocks of bs keys, [kb, ke) of them."""
+    ke = (Sk + bs - 1) // bs if ke is None else ke
+    return [np.arange(j * bs, min((j + 1) * bs, Sk)) for j in range(kb, ke)]
+
+
+def block_keys(B, Hq, Sq, Sk, d, causal, paged=False):
+    """Keys per score block of the kernel that runs this launch (256 for the
+    256-key kernel, else 128)."""
+    from attention_forward_blackwell_gb300 import binding
+    return binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, causal, 152,
+                                         paged=paged).keys_per_block
 
 
 def decode_warp_slices(k_lo, k_hi, warp):
@@ -176,10 +185,13 @@ def test_prefill_rebase_ramp(B, Hq, Hkv, S, d, causal, mode):
     assert binding.debug_prefill_plan(B, Hq, S, S, d, causal, n_sms)[2] == 1   # whole units
     x, scale = ramp_inputs(B, Hq, Hkv, S, S, d, tag=7000 + d + 3 * causal, mode=mode,
                            step_keys=128)
+    bs = block_keys(B, Hq, S, S, d, causal)
     t = scores_log2(x, scale, causal).reshape(-1, S)
-    n = lazy_rebases(t, prefill_blocks(S))
+    n = lazy_rebases(t, prefill_blocks(S, bs=bs))
+    # key blocks of the kernel, and 128-key ramp steps, that each row sees
+    vis_kblocks = np.array([len({j // bs for j in np.flatnonzero(np.isfinite(r))}) for r in t])
     vis_blocks = np.array([len({j // 128 for j in np.flatnonzero(np.isfinite(r))}) for r in t])
-    multi = vis_blocks >= 2
+    multi = vis_kblocks >= 2
     if mode == "steep":
         # every row that sees two or more key blocks moves its basis; with a
         # causal mask a row that sees only a few keys of its second block
@@ -201,12 +213,13 @@ def test_prefill_rebase_ramp(B, Hq, Hkv, S, d, causal, mode):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128, 256, 512])
-@pytest.mark.parametrize("pos", [200, 1000])
+@pytest.mark.parametrize("d", [64, 96, 128, 256, 512])
+@pytest.mark.parametrize("pos", [300, 1000])
 def test_prefill_dominant_key_in_a_later_block(d, causal, pos):
     """K*8 gives scores spread ~8.5 (max ~25 over 1,100 keys); key `pos`
-    (block 1 or the last block) scores ~60 for every query, so every row that
-    sees it jumps by more than 30 log2 units at that block and O ~ v_pos."""
+    (a middle block or the last block, for 128- and 256-key blocks alike)
+    scores ~60 for every query, so every row that sees it jumps by more than
+    30 log2 units at that block and O ~ v_pos."""
     from attention_forward_blackwell_gb300 import inputs
     S = 1100
     Hq = 2
@@ -216,7 +229,7 @@ def test_prefill_dominant_key_in_a_later_block(d, causal, pos):
     x.k[..., pos, 0] = 60.0 * math.sqrt(d) / 4.0
     scale = 1.0 / math.sqrt(d)
     t = scores_log2(x, scale, causal).reshape(-1, S)
-    n = lazy_rebases(t, prefill_blocks(S))
+    n = lazy_rebases(t, prefill_blocks(S, bs=block_keys(1, Hq, S, S, d, causal)))
     sees = np.isfinite(t[:, pos])
     assert n[sees].astype(bool).all() and sees.sum() >= Hq * (S - pos)
     o, lse = _run_prefill(x, scale, causal)
@@ -230,21 +243,25 @@ def test_prefill_dominant_key_in_a_later_block(d, causal, pos):
 
 
 @pytest.mark.parametrize("mode", ["steep", "mixed"])
-@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d", [
-    (1, 2, 2, 2048, 2048, 64),
-    (1, 2, 1, 2048, 2304, 96),
-    (1, 2, 2, 2048, 2048, 128),
-    (1, 2, 1, 1024, 2048, 256),
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,paged", [
+    (1, 2, 2, 2048, 2048, 64, False),
+    (1, 2, 1, 2048, 2304, 96, True),
+    (1, 2, 2, 2048, 2048, 128, True),
+    (1, 2, 1, 1024, 2048, 256, False),
 ], ids=["d64", "d96", "d128", "d256"])
-def test_split_unit_merge_rebases(B, Hq, Hkv, Sq, Sk, d, mode):
+def test_split_unit_merge_rebases(B, Hq, Hkv, Sq, Sk, d, paged, mode):
     """Query blocks computed in pieces along the key axis: with the ramp the
     later piece holds the larger scores (steep: every row's later piece beats
     the first by far more than 8 log2 units; mixed: in both directions), so
     the merge of the pieces rescales the earlier partial O and row_sum, and
-    every piece also rebases inside itself."""
+    every piece also rebases inside itself.  (Head_dim 96 and 128 split on
+    paged caches: their contiguous non-causal launches run the persistent
+    256-key kernel, which does not split.)"""
     from attention_forward_blackwell_gb300 import binding
+    from gpu_parity import to_pages
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    n_full, n_tail, split = binding.debug_prefill_plan(B, Hq, Sq, Sk, d, False, n_sms)
+    n_full, n_tail, split = binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, False, n_sms,
+                                                          paged=paged)[:3]
     assert n_full == 0 and split > 1, (n_full, n_tail, split)
     nk = (Sk + 127) // 128
     x, scale = ramp_inputs(B, Hq, Hkv, Sq, Sk, d, tag=7200 + d, mode=mode, step_keys=128)
@@ -261,7 +278,14 @@ def test_split_unit_merge_rebases(B, Hq, Hkv, Sq, Sk, d, mode):
         assert (jump[slope > 9] > THRESHOLD).all()
         # falling rows: the first piece dominates, the later ones are scaled down
         assert (piece_max[slope < -1, 0] > piece_max[slope < -1, -1] + 4).all()
-    o, lse = _run_prefill(x, scale, False)
+    if paged:
+        kc, vc, table, _ = to_pages(x.k, x.v, [Sk] * B, 256, seed=d)
+        lens = torch.full((B,), Sk, dtype=torch.int32, device="cuda")
+        o, lse = binding.prefill_paged(x.q, kc, vc, table, lens, scale=scale)
+        torch.cuda.synchronize()
+        check_device_error()
+    else:
+        o, lse = _run_prefill(x, scale, False)
     ro, rl = oracle_for(x, scale, False)
     compare(o, lse, ro, rl, f"split merge d={d} split={split} {mode}")
 

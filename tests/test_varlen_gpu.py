@@ -89,8 +89,12 @@ def test_prefill_varlen(Hq, Hkv, d, lens_q, lens_k, causal, window, sinks_on):
                                       threads=THREADS, window=window, sinks=sk_np)
         compare(o_b, l_b, ro, rl, f"varlen seq {b} (lq={lq}, lk={lk})")
         # the dense kernel on the sequence alone does the same arithmetic
-        # (no key-axis split: causal, windowed or fewer than 16 key blocks)
-        if causal or window > 0 or lk < 2048:
+        # (no key-axis split: causal, windowed or fewer than 16 key blocks;
+        # not the 256-key kernel, which takes dense non-causal head_dim-96 /
+        # 128 launches without a window)
+        same_kernel = binding.debug_prefill_plan_ex(
+            1, Hq, lq, lk, d, causal, 152, window=window).keys_per_block == 128
+        if same_kernel and (causal or window > 0 or lk < 2048):
             o2, l2 = binding.prefill(qb, kb, vb, scale=scale, causal=causal, window=window,
                                      sinks=sinks)
             torch.cuda.synchronize()
@@ -154,7 +158,7 @@ def test_prefill_varlen_paged(Hq, Hkv, d, P, lens_q, lens_k, causal):
     """Packed queries over shuffled, NaN-poisoned pages: each sequence against
     the oracle, and bit for bit against the packed-key path on the same keys."""
     from attention_forward_blackwell_gb300 import binding, inputs
-    from test_paged_gpu import to_pages
+    from gpu_parity import to_pages
     q, k, v, cq, ck = packed(lens_q, lens_k, Hq, Hkv, d, seed=7 * P + d)
     B, Sk = len(lens_k), max(lens_k)
     ks = np.concatenate([[0], np.cumsum(lens_k)])
