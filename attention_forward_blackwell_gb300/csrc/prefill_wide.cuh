@@ -33,8 +33,9 @@
 //               each block for all 128 rows (thread = row = TMEM lane); the
 //               two halves of a row exchange their block maxima through
 //               shared memory, then share one running max (the O basis);
-//   warps 8-11  correction: rebases O when the running max moved (lazily,
-//               as in the other kernels), and at a unit's end drains O / l
+//   warps 8-11  correction: follows the running max from the same block
+//               maxima, rebases O when it moved (lazily, as in the other
+//               kernels), and at a unit's end drains O / l
 //               to global memory through 2 KB staging buffers and TMA
 //               stores while the next unit's first scores run;
 //   warp 12     MMA issue (one lane): S(J+1), then PV(J);
@@ -49,10 +50,13 @@
 //
 // Barrier protocol (every wait bounded):
 //   s_full       S(J) complete (MMA commit), one phase per block;
-//   s_free       S(J) read into registers by both softmax warpgroups (8
-//                warps); S(J+1) waits for it;
-//   xm[J & 1]    both halves' block maxima of block J posted (8 warps);
-//   mb_full[J&1] rebase factor of block J posted (warpgroup 0);
+//   xm[J & 1]    both halves' block maxima of block J posted (8 warps),
+//                after each warp has read S(J) into registers: the softmax
+//                halves take the other half's max from it, the MMA lane
+//                issues S(J+1) into the score buffer after it, and the
+//                correction warpgroup derives the rebase factor of block J
+//                from the two maxima with the softmax's own operations (so
+//                no mailbox carries it);
 //   p_ready[J&1] P(J) written (8 softmax warps) and O rebased (4 correction
 //                warps); PV(J) waits for it;
 //   pv_done[J&1] PV(J) complete; P(J+1) is written only after it;
@@ -63,11 +67,14 @@
 //                warps); the next unit's first PV and final statistics wait
 //                for it.
 // A copy indexed by J & 1 is never two phases ahead of a reader: the
-// softmax posts block J+2's message after S(J+2) completed, which the MMA
-// lane issued after PV(J), which waited for P-ready(J), which includes the
-// correction's arrival for block J (made after it read message J); the
-// halves' maxima of block J+2 are posted after both halves passed block
-// J+1's exchange, hence read block J's values.
+// halves post block J+2's maxima after S(J+2) completed, which the MMA lane
+// issued after PV(J), which waited for P-ready(J), which includes the
+// correction's arrival for block J (made after it read block J's maxima);
+// the halves read the other's block-J max before they arrive for block
+// J+1, which the MMA lane waits for before S(J+2).  (Measured on GB300: the
+// rebase factor computed by the correction warpgroup instead of posted by
+// one softmax warpgroup, and no separate barrier for the score buffer, are
+// +2 to +4 %.)
 #pragma once
 
 namespace fa {
@@ -106,8 +113,8 @@ struct WideTraits {
     // register split of the 512 x 128 launch allocation: the two softmax
     // warpgroups, the correction warpgroup, the MMA / producer warpgroup
     static constexpr uint32_t LAUNCH_REGS = 128;
-    // (measured on GB300: 176 / 88 / 72, which removes 24 bytes of softmax
-    // spills, is 4-6 % slower)
+    // (measured on GB300: 176 / 88 / 72 and 176 / 96 / 64 are 4-6 % slower:
+    // the MMA-issue and producer warps need their 80)
     struct Regs {
         static constexpr uint32_t SOFTMAX = 168;
         static constexpr uint32_t CORR = 96;
@@ -129,9 +136,7 @@ struct WideAux {
     uint64_t bar_full[5];
     uint64_t bar_empty[5];
     uint64_t bar_s_full;
-    uint64_t bar_s_free;
     uint64_t bar_xm[2];
-    uint64_t bar_mb_full[2];
     uint64_t bar_p_ready[2];
     uint64_t bar_pv_done[2];
     uint64_t bar_fin;
@@ -142,9 +147,7 @@ struct WideAux {
     uint32_t tmem_base;
     int abort_flag;
     float xm[2][2][128];      // [J & 1][half][row] block maxima
-    float mb_alpha[2][128];   // [J & 1][row] rebase factor
     float mb_l[2][128];       // [half][row] row sums of the unit
-    float mb_m[128];          // running max of the unit
 };
 
 // Zeroes rows [r0, 128) of both 64-column chunks of a V slot (all 32 lanes
@@ -267,9 +270,9 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 }
 
 // MMA issue over the CTA's units (one lane).  Block J: S(J+1) once the
-// softmax has read S(J) out of the buffer (s_free) and K_{j+1} has landed,
-// then PV(J) once P(J) is ready.  Each ring slot is released by a commit
-// after the MMAs that read it.
+// softmax has read S(J) out of the buffer (both halves posted their block
+// maxima) and K_{j+1} has landed, then PV(J) once P(J) is ready.  Each ring
+// slot is released by a commit after the MMAs that read it.
 template <class T>
 __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem, uint32_t sQ,
                               uint32_t sRing, const WaitCtx& wc, unsigned long long* tr) {
@@ -297,8 +300,8 @@ __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem,
     auto score = [&](int J) -> bool {
         trace_mark(tr, kTrMma, J, 0);
         if (J > 0) {   // the softmax has read S(J-1) out of the buffer
-            if (!mbar_wait_lane(smem_u32(&aux->bar_s_free), (uint32_t)((J - 1) & 1), wc,
-                                kErrWaitTimeout | kSiteMmaSfree))
+            if (!mbar_wait_lane(smem_u32(&aux->bar_xm[(J - 1) & 1]), (uint32_t)(((J - 1) >> 1) & 1),
+                                wc, kErrWaitTimeout | kSiteMmaSfree))
                 return false;
             tc_fence_after();
         }
@@ -392,12 +395,13 @@ __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem,
 }
 
 // Softmax of one unit by warpgroup h (keys [128 h, 128 h + 128) of every
-// block; thread = row).  Per block: read the 128 scores, release the score
-// buffer, post the block max of the half and take the other half's, move
-// the running max lazily (the same rule as the other kernels), post the
-// rebase factor (warpgroup 0), compute P = exp2(s scale log2e - m) as bf16
-// and the half's row sum, then, once PV(J-1) has read the P buffer, store P.
-// Returns false if a wait gave up.
+// block; thread = row).  Per block: read the 128 scores, post the block max
+// of the half (which also releases the score buffer) and take the other
+// half's, move the running max lazily (the same rule as the other kernels;
+// the correction warpgroup follows it from the same maxima), compute
+// P = exp2(s scale log2e - m) as bf16 and the half's row sum, and store P
+// once PV(J-1) has read the P buffer.  At the unit's end the two halves'
+// row sums are posted for the epilogue.  Returns false if a wait gave up.
 template <class T>
 __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork& w,
                                   WideAux* aux, uint32_t tmem, const WaitCtx& wc, int J0, int kq,
@@ -425,8 +429,6 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
         for (int q = 0; q < 4; ++q) tmem_ld32(lane_base + T::S_COL + h * 128 + q * 32, u[q]);
         tmem_wait_ld();
         trace_mark(tr, trole, J, 1);
-        tc_fence_before();
-        mbar_arrive_warp(smem_u32(&aux->bar_s_free));   // S(J+1) may overwrite the buffer
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
@@ -447,6 +449,7 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
         const float mx_h = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
         trace_mark(tr, trole, J, 5);
         aux->xm[sb][h][r] = mx_h;
+        tc_fence_before();   // (this arrival also releases the score buffer to S(J+1))
         mbar_arrive_warp(smem_u32(&aux->bar_xm[sb]));
         if (!mbar_wait(smem_u32(&aux->bar_xm[sb]), par, wc, kErrWaitTimeout | kSiteSmXm))
             return false;
@@ -459,38 +462,42 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
             alpha = ex2_approx(m_run - m_new);   // 0 when m_run = -inf
             m_run = m_new;
         }
-        if (h == 0) {
-            aux->mb_alpha[sb][r] = alpha;
-            mbar_arrive_warp(smem_u32(&aux->bar_mb_full[sb]));
-        }
         // P(J) is computed into registers while PV(J-1) still reads P(J-1)
-        // out of the one P buffer; only its stores wait for PV(J-1)
+        // out of the one P buffer; only its stores wait for PV(J-1) (and
+        // storing the first half before computing the second keeps the
+        // registers within the softmax's share without spills: measured
+        // +0.5 % against storing both halves at the end)
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 nbase = make_float2(-base, -base);
         float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
         uint32_t pk[2][32];
+        const uint32_t pcol = lane_base + T::P_COL + h * 64;
+        // the first 64 keys' P, then (once PV(J-1) has completed: P(J)
+        // overwrites P(J-1)) their store while the other 64 are computed
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
             const float2 xv = ffma2(make_float2(s[2 * c], s[2 * c + 1]), sl2x2, nbase);
             const float2 pv = make_float2(ex2_approx(xv.x), ex2_approx(xv.y));
             rs[c & 3] = fadd2(rs[c & 3], pv);
             pk[c >> 5][c & 31] = pack_bf16x2(pv.x, pv.y);
+            if (c == 31) {
+                trace_mark(tr, trole, J, 3);
+                if (J > 0) {
+                    if (!mbar_wait(smem_u32(&aux->bar_pv_done[(J - 1) & 1]),
+                                   (uint32_t)(((J - 1) >> 1) & 1), wc,
+                                   kErrWaitTimeout | kSiteSmPv))
+                        return false;
+                    tc_fence_after();
+                }
+                trace_mark(tr, trole, J, 6);
+                tmem_st32(pcol, pk[0]);
+            }
         }
         const float2 rs01 = fadd2(rs[0], rs[1]), rs23 = fadd2(rs[2], rs[3]);
         const float2 rsum = fadd2(rs01, rs23);
         l_run = fmaf(l_run, alpha, rsum.x + rsum.y);
-        trace_mark(tr, trole, J, 3);
-        if (J > 0) {   // P(J) overwrites P(J-1): PV(J-1) must have completed
-            if (!mbar_wait(smem_u32(&aux->bar_pv_done[(J - 1) & 1]), (uint32_t)(((J - 1) >> 1) & 1),
-                           wc, kErrWaitTimeout | kSiteSmPv))
-                return false;
-            tc_fence_after();
-        }
-        trace_mark(tr, trole, J, 6);
-        const uint32_t pcol = lane_base + T::P_COL + h * 64;
-        tmem_st32(pcol, pk[0]);
         tmem_st32(pcol + 32, pk[1]);
         tmem_wait_st();
         tc_fence_before();
@@ -503,13 +510,13 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
                              kErrWaitTimeout | kSiteSmOdrained))
         return false;
     aux->mb_l[h][r] = l_run;
-    if (h == 0) aux->mb_m[r] = m_run;
     mbar_arrive_warp(smem_u32(&aux->bar_fin));
     return true;
 }
 
-// Correction of one unit (warpgroup CORR_WG, thread = row): rebases O
-// before PV(J) when the running max moved, then drains O / l (bf16) through
+// Correction of one unit (warpgroup CORR_WG, thread = row): follows the
+// running max from the halves' block maxima, rebases O before PV(J) when it
+// moved, then drains O / l (bf16) through
 // the warp's staging buffers and TMA stores (tm_o32: box {32, 32, 1}),
 // stores LSE = ln2 (m + log2 l) and arrives on O-drained.
 template <class T>
@@ -520,13 +527,22 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const int n = w.n_max;
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY;   // the softmax's running max, by the same operations
     for (int j = 0; j < n; ++j) {
         const int J = J0 + j;
         const int sb = J & 1;
-        if (!mbar_wait(smem_u32(&aux->bar_mb_full[sb]), (uint32_t)((J >> 1) & 1), wc,
+        // the halves' block maxima of block J, and the rebase factor the
+        // softmax derives from them
+        if (!mbar_wait(smem_u32(&aux->bar_xm[sb]), (uint32_t)((J >> 1) & 1), wc,
                        kErrWaitTimeout | kSiteCorrMbox))
             return false;
-        const float alpha = aux->mb_alpha[sb][r];
+        const float m_new = fmaxf(m_run, fmaxf(aux->xm[sb][0][r], aux->xm[sb][1][r]) * sl2);
+        float alpha = 1.f;
+        if (m_new > m_run + kRescaleThreshold) {
+            alpha = ex2_approx(m_run - m_new);   // 0 when m_run = -inf
+            m_run = m_new;
+        }
         if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
             // O must hold PV(J-1) before it is rebased
             if (!mbar_wait(smem_u32(&aux->bar_pv_done[(J - 1) & 1]),
@@ -550,7 +566,7 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
     if (!mbar_wait(smem_u32(&aux->bar_fin), (uint32_t)(kq & 1), wc, kErrWaitTimeout | kSiteEpiMbox))
         return false;
     const float l = aux->mb_l[0][r] + aux->mb_l[1][r];
-    const float m = aux->mb_m[r];
+    const float m = m_run;
     // O is final once PV(J0 + n - 1) completed (value MMAs into one
     // accumulator complete in issue order)
     const int Jl = J0 + n - 1;
@@ -597,10 +613,8 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
             mbar_init(smem_u32(&aux->bar_empty[i]), 1);
         }
         mbar_init(smem_u32(&aux->bar_s_full), 1);
-        mbar_init(smem_u32(&aux->bar_s_free), 8);          // 8 softmax warps
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&aux->bar_xm[i]), 8);       // 8 softmax warps
-            mbar_init(smem_u32(&aux->bar_mb_full[i]), 4);  // softmax warpgroup 0
             mbar_init(smem_u32(&aux->bar_p_ready[i]), 12); // 8 softmax + 4 correction warps
             mbar_init(smem_u32(&aux->bar_pv_done[i]), 1);
         }

@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("efb0b0ac1f6c8573a9e31313686f4bcdd278b9aa3fca235dbe34e00dea7e62a0",
-                "long_prefill_b1_h16_s8192_d128", 116495360),
+    "prefill": ("1fdd1a125fe70e31e10fbbda23dbf2f07e16b214f38b8eadac7f507b372dbe06",
+                "long_prefill_b1_h16_s8192_d128", 115543040),
     # captured at batch 16 (463.46 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
     "decode": ("3bb5ba0dff407b1f840b99a70421a37d3691925d34c0806be2ba6dbc45d87e0a",
