@@ -91,12 +91,11 @@ struct PrefillLaunch {
                                 // rows, tm_k box {64, 256, 1}, tm_o32 set)
 };
 
-// The 256-key persistent kernel (head_dim 96 and 128) takes dense launches
-// without a mask: no causal mask, no window, contiguous K/V (no block
-// table), no packed sequences.  (Causal launches measured 2-4 % faster on
-// the two-tile kernel: a 256-key block on the diagonal is up to half masked.)
-inline bool prefill_wide_ok(int head_dim, bool causal, int window, bool paged, bool packed) {
-    return (head_dim == 96 || head_dim == 128) && !causal && window <= 0 && !paged && !packed;
+// The 256-key persistent kernel (head_dim 96 and 128) takes dense launches,
+// causal or not: no window, contiguous K/V (no block table), no packed
+// sequences.
+inline bool prefill_wide_ok(int head_dim, int window, bool paged, bool packed) {
+    return (head_dim == 96 || head_dim == 128) && window <= 0 && !paged && !packed;
 }
 // Query rows of one prefill unit (query block) for a head dimension.
 inline int prefill_rows_per_cta(int head_dim) { return head_dim <= 128 ? 256 : 128; }
@@ -155,7 +154,7 @@ struct PrefillShape {
 inline PrefillShape prefill_shape(int batch, int hq, int sq, int sk, int head_dim, bool causal,
                                   int window, bool paged, bool packed, int num_sms) {
     PrefillShape s;
-    s.wide = prefill_wide_ok(head_dim, causal, window, paged, packed);
+    s.wide = prefill_wide_ok(head_dim, window, paged, packed);
     s.rows_per_unit = s.wide ? 128 : prefill_rows_per_cta(head_dim);
     s.keys_per_block = s.wide ? 256 : 128;
     s.num_mblk = (sq + s.rows_per_unit - 1) / s.rows_per_unit;

@@ -2170,7 +2170,8 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
         // dense, unmasked: 256-key score blocks, one persistent CTA per SM
         if (p.wide) {
             using W = WideTraits<D>;
-            const PrefillKernelFn kern = prefill_kernel_wide<D>;
+            const PrefillKernelFn kern =
+                p.causal ? prefill_kernel_wide<D, true> : prefill_kernel_wide<D, false>;
             cudaError_t e = cudaFuncSetAttribute(
                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W::SMEM_TOTAL);
             if (e != cudaSuccess) return e;

@@ -1,9 +1,8 @@
-// Prefill with 256-key score blocks (head_dim 96 and 128, no mask): one
-// persistent CTA per SM, one Q tile of 128 rows per unit.  Dense launches
-// without a causal mask, a window, paged caches or packed sequences run it;
-// the others run the two-tile kernels of prefill.cuh (causal launches
-// measured 2-4 % faster there: a 256-key block on the diagonal is up to half
-// masked work).
+// Prefill with 256-key score blocks (head_dim 96 and 128): one persistent
+// CTA per SM, one Q tile of 128 rows per unit.  Dense launches without a
+// window, paged caches or packed sequences run it, causal or not (causal
+// units come heaviest first, as in the other kernels); the others run the
+// two-tile kernels of prefill.cuh.
 //
 // Included by prefill.cuh after the roles and helpers it shares (the work
 // split, the staged O drain, the final normaliser).
@@ -79,8 +78,9 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool C = false>
 struct WideTraits {
+    static constexpr bool CAUSAL = C;               // causal mask (bottom-right aligned)
     static constexpr int BM = 128;                  // query rows of a unit = TMEM lanes
     static constexpr int BN = 256;                  // keys per score block
     static constexpr int NQ = 1;                    // (shared work split: one Q tile)
@@ -190,7 +190,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
         if (u >= a.n_full) break;
-        const PrefillWork w = prefill_work<T, false, false, false>(a, u);
+        const PrefillWork w = prefill_work<T, T::CAUSAL, false, false>(a, u);
         if (w.n_max <= 0) continue;
         const int plane = w.b * a.Hkv + w.hk;
         // next ring position's slot, once its previous contents were consumed
@@ -249,7 +249,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
             mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
             load_chunks<T, T::NCH>(sQ, tm_q, 0, w.row0, w.b * a.Hq + w.h, bar_q);
             const int un = persist_unit(i + 1, x, G);   // this CTA's next unit
-            if (un < a.n_full) prefetch_q_of<T, false, false, false>(tm_q, a, un);
+            if (un < a.n_full) prefetch_q_of<T, T::CAUSAL, false, false>(tm_q, a, un);
         }
         __syncwarp();
         ++kq;
@@ -329,7 +329,7 @@ __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem,
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
         if (u >= a.n_full) break;
-        const PrefillWork w = prefill_work<T, false, false, false>(a, u);
+        const PrefillWork w = prefill_work<T, T::CAUSAL, false, false>(a, u);
         const int n = w.n_max;
         if (n <= 0) continue;
         if (!mbar_wait_lane(smem_u32(&aux->bar_q), (uint32_t)(kq & 1), wc,
@@ -411,7 +411,8 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
     const int trole = h == 0 ? kTrSoftmax0 : kTrSoftmax1;
     const int r = (warp & 3) * 32 + lane;                    // row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int lim = w.L - 1;   // last visible key of every row (keys from the unit's first)
+    int lim = w.L - 1;   // last visible key of this row
+    if (T::CAUSAL) lim = min(lim, w.row0 + r + w.off);
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
     float l_run = 0.f;         // this half's running row sum in that basis
@@ -590,13 +591,13 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
     return true;
 }
 
-template <int D>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
     prefill_kernel_wide(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o32, const PrefillArgs args) {
-    using T = WideTraits<D>;
+    using T = WideTraits<D, CAUSAL>;
     static_assert(sizeof(WideAux) <= T::SMEM_AUX, "auxiliary shared block too large");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -645,7 +646,7 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
             if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
-            const PrefillWork w = prefill_work<T, false, false, false>(args, u);
+            const PrefillWork w = prefill_work<T, CAUSAL, false, false>(args, u);
             if (w.n_max <= 0) continue;
             if (!wide_softmax_unit<T>(wg, args, w, aux, tmem, wc, J0, kq, tr)) break;
             J0 += w.n_max;
@@ -657,7 +658,7 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
             if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
-            const PrefillWork w = prefill_work<T, false, false, false>(args, u);
+            const PrefillWork w = prefill_work<T, CAUSAL, false, false>(args, u);
             if (w.n_max <= 0) {
                 write_empty_unit<T>(args, w);
                 continue;

@@ -83,8 +83,8 @@ typedef enum fa_status {
  * CTA per SM processes the query blocks in turn instead (heaviest first over
  * the SMs, keeping its pipeline state from one block to the next and
  * storing each block's O while the next one starts).  At head_dim 96 and 128
- * without a causal mask (also without a window, paged caches or packed
- * sequences), a persistent kernel with 256-key score blocks and query blocks
+ * without a window, paged caches or packed sequences (causal or not), a
+ * persistent kernel with 256-key score blocks and query blocks
  * of 128 rows runs instead: one N = 256 score MMA per K-step, P in tensor
  * memory columns of its own, the next block's score MMA issued while the
  * softmax of this one runs, each row's softmax split over two warpgroups

@@ -166,7 +166,7 @@ def test_wait_timeout_selftest_reports_and_recovers():
 @pytest.mark.parametrize("B,Hq,Sq,Sk,d,causal", [
     (1, 1, 128, 128, 64, False),    # one key tile per query tile
     (1, 1, 257, 1, 64, False),      # one key, a CTA whose second tile has no rows
-    (1, 2, 300, 300, 128, True),    # the two query tiles finish after different counts
+    (1, 2, 300, 300, 128, True),    # causal 256-key kernel: units of 1 and 2 blocks
     (1, 4, 600, 200, 256, True),    # d = 256, rows that see no key
 ])
 def test_barrier_protocol_stress(B, Hq, Sq, Sk, d, causal):

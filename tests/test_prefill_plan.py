@@ -35,8 +35,9 @@ KINDS = [
 
 
 def _wide(d, causal, window, paged, packed):
-    """The 256-key persistent kernel: head_dim 96 / 128, dense, unmasked."""
-    return d in (96, 128) and not causal and window <= 0 and not paged and not packed
+    """The 256-key persistent kernel: head_dim 96 / 128, dense, no window
+    (causal or not)."""
+    return d in (96, 128) and window <= 0 and not paged and not packed
 
 
 @pytest.mark.parametrize("kind", KINDS, ids=[str(k) for k in KINDS])
@@ -82,11 +83,13 @@ def test_dense_plan_is_the_extended_one(shape):
 
 def test_plan_of_the_bench_workloads():
     plan = binding.debug_prefill_plan_ex
-    # non-causal head_dim 128: 256-key kernel, 1024 units of 128 rows, persistent
+    # head_dim 128: 256-key kernel, 1024 units of 128 rows, persistent
     assert plan(2, 16, 4096, 4096, 128, False, 152) == (1024, 0, 1, 128, 256, True)
     assert plan(1, 16, 8192, 8192, 128, False, 152) == (1024, 0, 1, 128, 256, True)
-    # causal: two-tile kernel, heaviest first, one CTA per unit
-    assert plan(2, 16, 4096, 4096, 128, True, 152) == (512, 0, 1, 256, 128, False)
+    # causal: the same kernel, heaviest-first units
+    assert plan(2, 16, 4096, 4096, 128, True, 152) == (1024, 0, 1, 128, 256, True)
+    # with a window: two-tile kernel, one CTA per unit
+    assert plan(2, 16, 4096, 4096, 128, True, 152, window=1024) == (512, 0, 1, 256, 128, False)
     # the same non-causal problem on paged caches: the last wave split in two
     assert plan(2, 16, 4096, 4096, 128, False, 152, paged=True) == (456, 56, 2, 256, 128, False)
     # causal GQA head_dim 256: persistent over 2048 units

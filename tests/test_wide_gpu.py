@@ -1,5 +1,5 @@
-"""The persistent 256-key prefill kernel (head_dim 96 and 128, dense,
-non-causal, no window) against the fp64 oracle.
+"""The persistent 256-key prefill kernel (head_dim 96 and 128, dense, no
+window, causal or not) against the fp64 oracle.
 
 One CTA per SM walks units of 128 query rows; each score block is 256 keys
 (one N = 256 score MMA per K-step), the two softmax warpgroups take 128 keys
@@ -8,9 +8,10 @@ and the next block's score MMA runs during the softmax ("b200-flash-attention4-
 planner" A1, E.3-E.8).  These shapes exercise: ragged query and key lengths
 (a last block of 1 key, a value half with no valid key), per-sequence key
 lengths with NaN padding and empty sequences (units written as O = 0,
-LSE = -inf), one query row, one key, GQA, attention sinks, many units per CTA
-(running barrier phases over the CTA's units), repeated launches and a CUDA
-graph replay.
+LSE = -inf), one query row, one key, GQA, attention sinks, the causal mask
+(bottom-right aligned, with rows that see no key when Sq > Sk), many units
+per CTA (running barrier phases over the CTA's units, heaviest-first causal
+units), repeated launches and a CUDA graph replay.
 """
 import math
 
@@ -33,17 +34,17 @@ def built():
     free_cuda()
 
 
-def _assert_wide(B, Hq, Sq, Sk, d):
+def _assert_wide(B, Hq, Sq, Sk, d, causal=False):
     from attention_forward_blackwell_gb300 import binding
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    p = binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, False, n_sms)
+    p = binding.debug_prefill_plan_ex(B, Hq, Sq, Sk, d, causal, n_sms)
     assert p.keys_per_block == 256 and p.rows_per_unit == 128 and p.persistent, p
     return p
 
 
-def _run(x, scale, sinks=None):
+def _run(x, scale, sinks=None, causal=False):
     from attention_forward_blackwell_gb300 import binding
-    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=False, seqlens_k=x.seqlens_k,
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k,
                              sinks=sinks)
     torch.cuda.synchronize()
     check_device_error()
@@ -61,24 +62,25 @@ FULL = [
 ]
 
 
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,lengths", FULL,
                          ids=[f"b{c[0]}h{c[1]}x{c[2]}q{c[3]}k{c[4]}d{c[5]}" for c in FULL])
-def test_every_element(B, Hq, Hkv, Sq, Sk, d, lengths):
+def test_every_element(B, Hq, Hkv, Sq, Sk, d, lengths, causal):
     from attention_forward_blackwell_gb300 import inputs
-    _assert_wide(B, Hq, Sq, Sk, d)
+    _assert_wide(B, Hq, Sq, Sk, d, causal)
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=1500 + Sq + d, device="cuda",
                            lengths=lengths)
     if lengths is not None:
         inputs.poison_beyond_lengths(x.k, x.seqlens_k)
         inputs.poison_beyond_lengths(x.v, x.seqlens_k)
     scale = 1.0 / math.sqrt(d)
-    o, lse = _run(x, scale)
+    o, lse = _run(x, scale, causal=causal)
     if lengths is not None:
         for b, L in enumerate(lengths):
             if L == 0:
                 assert torch.all(o[b] == 0) and torch.all(torch.isneginf(lse[b]))
-    ro, rl = oracle_for(x, scale, False)
-    compare(o, lse, ro, rl, f"256-key kernel {B, Hq, Hkv, Sq, Sk, d}")
+    ro, rl = oracle_for(x, scale, causal)
+    compare(o, lse, ro, rl, f"256-key kernel {B, Hq, Hkv, Sq, Sk, d} causal={causal}")
     free_cuda()
 
 
@@ -89,21 +91,23 @@ MANY = [
 ]
 
 
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,Hq,Hkv,S,d", MANY, ids=[f"b{c[0]}h{c[1]}s{c[3]}d{c[4]}" for c in MANY])
-def test_many_units_per_cta(B, Hq, Hkv, S, d):
+def test_many_units_per_cta(B, Hq, Hkv, S, d, causal):
     """Sampled rows (unit edges of a few heads plus random rows) against the
     oracle, and the first and last head in full."""
     from attention_forward_blackwell_gb300 import inputs
-    p = _assert_wide(B, Hq, S, S, d)
+    p = _assert_wide(B, Hq, S, S, d, causal)
     assert p.n_full > 4 * torch.cuda.get_device_properties(0).multi_processor_count
     x = inputs.make_inputs(B, Hq, Hkv, S, S, d, tag=1600 + d, device="cuda")
     scale = 1.0 / math.sqrt(d)
-    o, lse = _run(x, scale)
+    o, lse = _run(x, scale, causal=causal)
     rows = np.unique(np.concatenate([sample_rows(B, Hq, S, n_random=400, seed=S + d),
                                      np.arange(S), np.arange(B * Hq * S - S, B * Hq * S)]))
-    ro, rl = oracle_for(x, scale, False, rows=rows)
+    ro, rl = oracle_for(x, scale, causal, rows=rows)
     idx = torch.from_numpy(rows).cuda()
-    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, f"many units {B, Hq, Hkv, S, d}")
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl,
+            f"many units {B, Hq, Hkv, S, d} causal={causal}")
     del x, o, lse
     free_cuda()
 
