@@ -2167,7 +2167,7 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
         }
     }
     if constexpr (D == 96 || D == 128) {
-        // dense, unmasked: 256-key score blocks, one persistent CTA per SM
+        // dense, no window: 256-key score blocks, one persistent CTA per SM
         if (p.wide) {
             using W = WideTraits<D>;
             const PrefillKernelFn kern =

@@ -78,6 +78,8 @@
 
 namespace fa {
 
+constexpr int kWideSlots = 5;   // ring slots of the 256-key kernel
+
 template <int D, bool C = false>
 struct WideTraits {
     static constexpr bool CAUSAL = C;               // causal mask (bottom-right aligned)
@@ -95,7 +97,7 @@ struct WideTraits {
     static constexpr int KP = NCH;                  // slots of a K block: one chunk of 256 rows each
     static constexpr int VP = 2;                    // slots of a V block: 128 keys x NCH chunks each
     static constexpr int VKEYS = BN / VP;
-    static constexpr int NSLOT = 5;
+    static constexpr int NSLOT = kWideSlots;
     static constexpr int THREADS = 512;
     static constexpr int CORR_WG = 2;
     static constexpr int MMA_WARP = 12;
@@ -133,8 +135,8 @@ struct WideTraits {
 
 struct WideAux {
     uint64_t bar_q;
-    uint64_t bar_full[5];
-    uint64_t bar_empty[5];
+    uint64_t bar_full[kWideSlots];
+    uint64_t bar_empty[kWideSlots];
     uint64_t bar_s_full;
     uint64_t bar_xm[2];
     uint64_t bar_p_ready[2];
