@@ -63,8 +63,8 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("5754d9234c18b02f8392ee747eeccbff3f9ac2da0738771787bf6cff34906806",
-                "long_prefill_b1_h16_s8192_d128", 115750400),
+    "prefill": ("943cb0505a85c241125551eb78df1728c356549e2c887990598d1ece054ff8e2",
+                "long_prefill_b1_h16_s8192_d128", 115654400),
     # captured at batch 16 (463.46 MB, 1.016 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
     "decode": ("3bb5ba0dff407b1f840b99a70421a37d3691925d34c0806be2ba6dbc45d87e0a",
