@@ -9,7 +9,8 @@ planner" A1, E.3-E.8).  These shapes exercise: ragged query and key lengths
 (a last block of 1 key, a value half with no valid key), per-sequence key
 lengths with NaN padding and empty sequences (units written as O = 0,
 LSE = -inf), one query row, one key, GQA, attention sinks, the causal mask
-(bottom-right aligned, with rows that see no key when Sq > Sk), many units
+(bottom-right aligned, with rows that see no key when Sq > Sk), 24 seeded
+random shapes (head_dim, GQA ratio, ragged lengths, causal), many units
 per CTA (running barrier phases over the CTA's units, heaviest-first causal
 units), repeated launches and a CUDA graph replay.
 """
@@ -178,4 +179,46 @@ def test_replay_in_a_cuda_graph():
         torch.cuda.synchronize()
         check_device_error()
         assert torch.equal(o, o_ref) and torch.equal(lse, l_ref)
+    free_cuda()
+
+
+def _random_cases(n, seed):
+    """Seeded random small shapes for the 256-key kernel: head_dim 96 / 128,
+    causal or not, GQA ratio 1-4, Sq and Sk from 1 to 1,500 (ragged against
+    the 128-row units and 256-key blocks), optional per-sequence key lengths
+    with zeros."""
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for _ in range(n):
+        d = rng.choice([96, 128])
+        hkv = rng.choice([1, 2])
+        hq = hkv * rng.choice([1, 2, 4])
+        B = rng.choice([1, 2, 3])
+        sq = rng.randint(1, 1500)
+        sk = rng.randint(1, 1500)
+        lens = None
+        if rng.random() < 0.4:
+            lens = [rng.choice([0, rng.randint(1, sk), sk]) for _ in range(B)]
+        cases.append((B, hq, hkv, sq, sk, d, rng.random() < 0.5, lens))
+    return cases
+
+
+RANDOM = _random_cases(24, seed=2026)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,causal,lengths", RANDOM,
+                         ids=[f"r{i}" for i in range(len(RANDOM))])
+def test_random_shapes_every_element(B, Hq, Hkv, Sq, Sk, d, causal, lengths):
+    from attention_forward_blackwell_gb300 import inputs
+    _assert_wide(B, Hq, Sq, Sk, d, causal)
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=2000 + Sq + Sk, device="cuda",
+                           lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(x, scale, causal=causal)
+    ro, rl = oracle_for(x, scale, causal)
+    compare(o, lse, ro, rl, f"random {B, Hq, Hkv, Sq, Sk, d} causal={causal} lengths={lengths}")
     free_cuda()
