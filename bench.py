@@ -65,10 +65,10 @@ CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
     "prefill": ("943cb0505a85c241125551eb78df1728c356549e2c887990598d1ece054ff8e2",
                 "long_prefill_b1_h16_s8192_d128", 115654400),
-    # captured at batch 16 (463.46 MB, 1.016 x its algorithmic bytes) and
+    # captured at batch 16 (463.78 MB, 1.017 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
-    "decode": ("3bb5ba0dff407b1f840b99a70421a37d3691925d34c0806be2ba6dbc45d87e0a",
-               "decode_gqa_b64_hq64_hkv8_d128", 2204477584),
+    "decode": ("b3d5f849c25e7011fb921fdf56efe964d17581b057432e737006646007fd9890",
+               "decode_gqa_b64_hq64_hkv8_d128", 2206020388),
 }
 
 
