@@ -50,6 +50,7 @@ SIGNATURES = {
     "fa_selftest_exp2_poly": (_I, [_VP, _VP, _I, _VP]),
     "fa_debug_prefill_plan": (_I, [_I, _I, _I, _I, _I, _I, _I, _VP]),
     "fa_debug_prefill_plan_ex": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
+    "fa_debug_prefill_plan_gqa": (_I, [_I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _VP]),
     "fa_version": (_I, []),
 }
 
@@ -386,6 +387,24 @@ def debug_prefill_plan_ex(batch, hq, sq, sk, head_dim, causal, num_sms, *, windo
     if st != FA_OK:
         raise FaError(st, "fa_debug_prefill_plan_ex")
     return PrefillPlan(*out[:5], bool(out[5]))
+
+
+PrefillPlanGqa = collections.namedtuple(
+    "PrefillPlanGqa", "n_full n_tail split rows_per_unit keys_per_block persistent pack")
+
+
+def debug_prefill_plan_gqa(batch, hq, hkv, sq, sk, head_dim, causal, num_sms, *, window=0,
+                           paged=False, packed=False):
+    """The prefill work split with the kv head count: pack = query heads per
+    unit of the 256-key kernel (host only, see fa.h)."""
+    out = (ctypes.c_int * 7)()
+    st = lib().fa_debug_prefill_plan_gqa(int(batch), int(hq), int(hkv), int(sq), int(sk),
+                                         int(head_dim), int(bool(causal)), int(window),
+                                         int(bool(paged)), int(bool(packed)), int(num_sms),
+                                         ctypes.addressof(out))
+    if st != FA_OK:
+        raise FaError(st, "fa_debug_prefill_plan_gqa")
+    return PrefillPlanGqa(*out[:5], bool(out[5]), out[6])
 
 
 def selftest_exp2_poly(x, stream=None):

@@ -90,17 +90,18 @@ unsigned long long next_prefill_epoch() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 3-D bf16 map {d, rows, planes} with a {64, box_rows, 1} box (128 rows, or
-// 256 for the K blocks of the 256-key kernels) and 128-byte swizzle (rows
+// 3-D bf16 map {d, rows, planes} with a {64, box_rows, box_planes} box (128
+// rows of one plane; 256 rows for the K blocks of the 256-key kernels; 128 /
+// P rows of P planes for a head-packed Q tile) and 128-byte swizzle (rows
 // past `rows` and columns past `d` read as zero).
 // Strides in bytes: row_stride between rows, plane_stride between planes
 // (contiguous [planes][rows][d] when they are d * 2 and rows * d * 2).
 bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows, long long planes,
                         unsigned long long row_stride, unsigned long long plane_stride,
-                        unsigned box_rows = 128) {
+                        unsigned box_rows = 128, unsigned box_planes = 1) {
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
     const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)plane_stride};
-    const cuuint32_t box[3] = {64, box_rows, 1};
+    const cuuint32_t box[3] = {64, box_rows, box_planes};
     const cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -108,15 +109,17 @@ bool encode_map_strided(CUtensorMap* m, const void* base, int d, long long rows,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D bf16 map {d, rows, planes} with a {32, 32, 1} box and 64-byte swizzle
-// (16-byte chunks of each 64-byte row XOR-ed with bits 1-2 of the row): the
-// persistent head_dim-256 kernel's O stores from 2 KB per-warp staging areas.
+// 3-D bf16 map {d, rows, planes} with a {32, box_rows, 32 / box_rows} box
+// (32 rows in all) and 64-byte swizzle (16-byte chunks of each 64-byte row
+// XOR-ed with bits 1-2 of the row): the persistent kernels' O stores from
+// 2 KB per-warp staging areas; 16 rows x 2 planes for a head-packed tile of
+// 16 rows per head.
 bool encode_map32_strided(CUtensorMap* m, const void* base, int d, long long rows,
                           long long planes, unsigned long long row_stride,
-                          unsigned long long plane_stride) {
+                          unsigned long long plane_stride, unsigned box_rows = 32) {
     const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)planes};
     const cuuint64_t strides[2] = {(cuuint64_t)row_stride, (cuuint64_t)plane_stride};
-    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t box[3] = {32, box_rows, 32 / box_rows};
     const cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
@@ -316,8 +319,13 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     // kernel family, unit and block sizes, work split (head_dim 96 / 128,
     // dense and unmasked: the 256-key kernel)
     const PrefillShape shape = prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, window,
-                                             block_table != nullptr, vl != nullptr, di->num_sms);
+                                             block_table != nullptr, vl != nullptr, di->num_sms,
+                                             hq / hkv);
     const bool wide = shape.wide;
+    // head-packed tiles: Q boxes of R rows x P heads, O boxes of 32 rows
+    // (16 x 2 heads when R = 16)
+    const unsigned pack_rows = (unsigned)shape.rows_per_unit;
+    const unsigned o_box_rows = shape.pack > 1 && pack_rows < 32 ? pack_rows : 32;
     // Q, O: token-major packed tensors (map {d, tokens, heads}, a token's
     // heads adjacent) or dense [B, Hq, Sq, d]; K, V: paged caches, packed or
     // dense
@@ -326,12 +334,16 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
         if (!prefill_load_map(&p.tm_q, q, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes) ||
             !encode_map_strided(&p.tm_o, o, head_dim, vl->total_q, hq, row_bytes * hq, row_bytes))
             return FA_ERR_INVALID_ARG;
-    } else if (!prefill_load_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq, row_bytes,
-                                 row_bytes * sq) ||
+    } else if (!(shape.pack > 1
+                     ? encode_map_strided(&p.tm_q, q, head_dim, sq, (long long)batch * hq,
+                                          row_bytes, row_bytes * sq, pack_rows,
+                                          (unsigned)shape.pack)
+                     : prefill_load_map(&p.tm_q, q, head_dim, sq, (long long)batch * hq,
+                                        row_bytes, row_bytes * sq)) ||
                !encode_map(&p.tm_o, o, head_dim, sq, (long long)batch * hq) ||
                ((head_dim == 256 || wide) &&
                 !encode_map32_strided(&p.tm_o32, o, head_dim, sq, (long long)batch * hq,
-                                      row_bytes, row_bytes * sq))) {
+                                      row_bytes, row_bytes * sq, o_box_rows))) {
         return FA_ERR_INVALID_ARG;
     }
     if (block_table) {
@@ -372,6 +384,7 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     a.Sk = sk;
     a.group = hq / hkv;
     a.num_mblk = shape.num_mblk;
+    a.pack = shape.pack;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.wait_limit_ns = kWaitLimitNs;
     // head_dim 256: the producer of each CTA also prefetches into L2 the Q
@@ -625,14 +638,15 @@ fa_status fa_debug_prefill_trace(unsigned long long* buf, int block) {
     return FA_OK;
 }
 
-fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_dim, int causal,
-                                   int window, int paged, int packed, int num_sms, int* out) {
-    if (!out || batch <= 0 || hq <= 0 || sq <= 0 || sk <= 0 || batch > 65535 || hq > 65535 ||
-        num_sms < 1)
+fa_status fa_debug_prefill_plan_gqa(int batch, int hq, int hkv, int sq, int sk, int head_dim,
+                                    int causal, int window, int paged, int packed, int num_sms,
+                                    int* out) {
+    if (!out || batch <= 0 || hq <= 0 || hkv <= 0 || hq % hkv != 0 || sq <= 0 || sk <= 0 ||
+        batch > 65535 || hq > 65535 || num_sms < 1)
         return FA_ERR_INVALID_ARG;
     if (!prefill_head_dim_ok(head_dim)) return FA_ERR_INVALID_ARG;
     const PrefillShape sh = prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, window,
-                                          paged != 0, packed != 0, num_sms);
+                                          paged != 0, packed != 0, num_sms, hq / hkv);
     if (sh.units * prefill_ctas_per_unit(head_dim) >= (1ll << 31)) return FA_ERR_INVALID_ARG;
     out[0] = sh.plan.n_full;
     out[1] = sh.plan.n_tail;
@@ -640,6 +654,18 @@ fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_d
     out[3] = sh.rows_per_unit;
     out[4] = sh.keys_per_block;
     out[5] = sh.persistent ? 1 : 0;
+    out[6] = sh.pack;
+    return FA_OK;
+}
+
+fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_dim, int causal,
+                                   int window, int paged, int packed, int num_sms, int* out) {
+    if (!out) return FA_ERR_INVALID_ARG;
+    int full[7];
+    const fa_status st = fa_debug_prefill_plan_gqa(batch, hq, hq > 0 ? hq : 1, sq, sk, head_dim,
+                                                   causal, window, paged, packed, num_sms, full);
+    if (st != FA_OK) return st;
+    for (int i = 0; i < 6; ++i) out[i] = full[i];
     return FA_OK;
 }
 

@@ -45,6 +45,12 @@ struct PrefillArgs {
     const int* cu_seqlens_k;
     int total_q, total_k;
     int num_mblk;               // query blocks (units) per (b, h)
+    // Query heads per tile of the 256-key kernel (1: one head per unit).
+    // With pack = P > 1 a unit's 128 tile rows are P consecutive query heads
+    // of one kv group x 128 / P query positions (row r: head h + r / (128 / P),
+    // position row0 + r % (128 / P)), and num_mblk counts units per (b, group
+    // of P heads).
+    int pack;
     // Work split (see prefill_work): CTAs [0, n_full) process whole units;
     // each later unit is split into `split` pieces of its nk key blocks.
     int n_full;
@@ -97,6 +103,18 @@ struct PrefillLaunch {
 inline bool prefill_wide_ok(int head_dim, int window, bool paged, bool packed) {
     return (head_dim == 96 || head_dim == 128) && window <= 0 && !paged && !packed;
 }
+// Query heads that share one 128-row tile of the 256-key kernel (GQA head
+// packing): rows per head R = the next power of two >= sq, at least 16, and
+// P = 128 / R heads of the group (P a power of two dividing it); short query
+// lengths then fill the tile with the group's other heads, which read the
+// same keys, instead of leaving most of its rows empty.
+inline int prefill_pack(int sq, int group) {
+    int rows = 16;
+    while (rows < sq && rows < 128) rows *= 2;
+    int p = 128 / rows;
+    while (p > 1 && (group % p) != 0) p /= 2;
+    return p;
+}
 // Query rows of one prefill unit (query block) for a head dimension.
 inline int prefill_rows_per_cta(int head_dim) { return head_dim <= 128 ? 256 : 128; }
 // CTAs per unit: head_dim 512 shares the output columns out over two.
@@ -142,7 +160,8 @@ inline PrefillPlan plan_prefill(long long units, int nk, int causal, int ctas) {
 // function serves the launch and the plan queries, so that they agree.
 struct PrefillShape {
     bool wide;             // prefill_wide_ok: the 256-key persistent kernel
-    int rows_per_unit;     // query rows of a unit (query block)
+    int pack;              // query heads per unit (prefill_pack; 1 unless wide)
+    int rows_per_unit;     // query rows of a unit (query block), per head
     int keys_per_block;    // keys of a score block
     int num_mblk;          // units per (batch entry, query head)
     long long units;
@@ -151,14 +170,17 @@ struct PrefillShape {
     bool persistent;       // one CTA per SM walks the unit list
 };
 
+// group: query heads per kv head (1: no head packing).
 inline PrefillShape prefill_shape(int batch, int hq, int sq, int sk, int head_dim, bool causal,
-                                  int window, bool paged, bool packed, int num_sms) {
+                                  int window, bool paged, bool packed, int num_sms,
+                                  int group = 1) {
     PrefillShape s;
     s.wide = prefill_wide_ok(head_dim, window, paged, packed);
-    s.rows_per_unit = s.wide ? 128 : prefill_rows_per_cta(head_dim);
+    s.pack = s.wide ? prefill_pack(sq, group > 0 ? group : 1) : 1;
+    s.rows_per_unit = s.wide ? 128 / s.pack : prefill_rows_per_cta(head_dim);
     s.keys_per_block = s.wide ? 256 : 128;
     s.num_mblk = (sq + s.rows_per_unit - 1) / s.rows_per_unit;
-    s.units = (long long)batch * hq * s.num_mblk;
+    s.units = (long long)batch * (hq / s.pack) * s.num_mblk;
     s.nk = (sk + s.keys_per_block - 1) / s.keys_per_block;
     // not split: causal units (heaviest first), windowed ones (fewer key
     // blocks than nk), packed sequences (units of different lengths), head_dim

@@ -2172,8 +2172,13 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
         // dense, no window: 256-key score blocks, one persistent CTA per SM
         if (p.wide) {
             using W = WideTraits<D>;
+            // (head-packed GQA tiles: an instance of their own)
             const PrefillKernelFn kern =
-                p.causal ? prefill_kernel_wide<D, true> : prefill_kernel_wide<D, false>;
+                p.args.pack > 1
+                    ? (p.causal ? prefill_kernel_wide<D, true, true>
+                                : prefill_kernel_wide<D, false, true>)
+                    : (p.causal ? prefill_kernel_wide<D, true, false>
+                                : prefill_kernel_wide<D, false, false>);
             cudaError_t e = cudaFuncSetAttribute(
                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W::SMEM_TOTAL);
             if (e != cudaSuccess) return e;

@@ -7,6 +7,17 @@
 // Included by prefill.cuh after the roles and helpers it shares (the work
 // split, the staged O drain, the final normaliser).
 //
+// GQA head packing (PACK instances, PrefillArgs::pack = P > 1): with short
+// queries the 128 tile rows hold P query heads of one kv group x 128 / P
+// positions ("b200-flash-attention4-planner" E.7: explicit head mapping and
+// reuse), so that one stream of K/V tiles serves all P heads instead of a
+// tile whose rows are mostly empty.  The Q map's box is {64, 128 / P, P}
+// (the P heads' rows land in shared memory head after head, exactly the
+// unpacked tile's layout), the O map's box {32, 16, 2} when a head has 16
+// rows; the causal mask, the sink and the LSE take each row's own head and
+// position (wide_row).  Measured on GB300 (B=64 Hq=32 Hkv=4, 16 queries
+// over 4,096 keys): 93 -> 335 TFLOPS causal, 192 -> 671 non-causal.
+//
 // Why: from one issuing thread a tcgen05.mma of M = 128, K = 16 occupies
 // the tensor pipe ~80 cycles for any N up to 128 and 128 cycles at N = 256
 // (measured on GB300), so only N = 256 runs at the pipe's full rate.  The
@@ -80,9 +91,10 @@ namespace fa {
 
 constexpr int kWideSlots = 5;   // ring slots of the 256-key kernel
 
-template <int D, bool C = false>
+template <int D, bool C = false, bool PK = false>
 struct WideTraits {
     static constexpr bool CAUSAL = C;               // causal mask (bottom-right aligned)
+    static constexpr bool PACK = PK;                // GQA head packing (PrefillArgs::pack > 1)
     static constexpr int BM = 128;                  // query rows of a unit = TMEM lanes
     static constexpr int BN = 256;                  // keys per score block
     static constexpr int NQ = 1;                    // (shared work split: one Q tile)
@@ -152,6 +164,96 @@ struct WideAux {
     float mb_l[2][128];       // [half][row] row sums of the unit
 };
 
+// Unit u of the 256-key kernel.  Without packing, prefill_work's unit
+// (batch entry, query head, block of 128 query rows).  With P = a.pack heads
+// per tile: (batch entry, heads h .. h + P - 1 of one kv group, block of
+// R = 128 / P query positions), ordered as prefill_work orders its units
+// (causal: query block slowest, heaviest first); row0 is the block's first
+// position, and the key blocks are those its last position sees.
+template <class T>
+__device__ __forceinline__ PrefillWork wide_work(const PrefillArgs& a, int u) {
+    if constexpr (!T::PACK) {
+        return prefill_work<T, T::CAUSAL, false, false>(a, u);
+    } else {
+        PrefillWork w;
+        const int rows = T::BM / a.pack;            // query positions per head
+        const int ng = a.Hq / a.pack;               // head groups per batch entry
+        const int nbh = a.B * ng;
+        const int x = T::CAUSAL ? u / nbh : u % a.num_mblk;
+        const int hb = T::CAUSAL ? u % nbh : u / a.num_mblk;
+        const int mblk = T::CAUSAL ? (a.num_mblk - 1 - x) : x;
+        w.b = hb / ng;
+        w.h = (hb % ng) * a.pack;
+        w.hk = w.h / a.group;
+        int L = a.Sk;
+        if (a.seqlens_k != nullptr) L = max(0, min(a.seqlens_k[w.b], a.Sk));
+        w.L = L;
+        w.off = L - a.Sq;
+        w.row0 = mblk * rows;
+        int last = L - 1;   // last key any row of the tile can see
+        if (T::CAUSAL) last = min(last, w.row0 + rows - 1 + w.off);
+        const int n = last >= 0 ? last / T::BN + 1 : 0;
+        w.kb = 0;
+        w.n_kv[0] = w.n_kv[1] = n;
+        w.n_max = n;
+        w.piece = -1;
+        w.tail = -1;
+        w.Lq = w.q0 = w.k0 = 0;
+        w.dv0 = 0;
+        return w;
+    }
+}
+
+// Query head and position of tile row r of unit w.
+template <class T>
+__device__ __forceinline__ void wide_row(const PrefillArgs& a, const PrefillWork& w, int r,
+                                         int& h, int& pos) {
+    if constexpr (T::PACK) {
+        const int rows = T::BM / a.pack;
+        h = w.h + r / rows;
+        pos = w.row0 + r % rows;
+    } else {
+        h = w.h;
+        pos = w.row0 + r;
+    }
+}
+
+// L2 prefetch of unit u's Q tile (the Q map's box: 128 rows of one head, or
+// R rows x P heads).
+template <class T>
+__device__ __forceinline__ void wide_prefetch_q(const CUtensorMap* tm_q, const PrefillArgs& a,
+                                                int u) {
+    if constexpr (!T::PACK) {
+        prefetch_q_of<T, T::CAUSAL, false, false>(tm_q, a, u);
+    } else {
+        const PrefillWork w2 = wide_work<T>(a, u);
+        if (w2.n_max <= 0) return;
+#pragma unroll
+        for (int c = 0; c < T::NCH; ++c)
+            tma_prefetch_l2_3d(tm_q, c * 64, w2.row0, w2.b * a.Hq + w2.h);
+    }
+}
+
+// A unit without keys: O = 0 and LSE = log of the sink term (or -inf), by
+// the correction warpgroup (thread = row).
+template <class T>
+__device__ void wide_write_empty(const PrefillArgs& a, const PrefillWork& w) {
+    if constexpr (!T::PACK) {
+        write_empty_unit<T>(a, w);
+    } else {
+        const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);
+        int h, pos;
+        wide_row<T>(a, w, r, h, pos);
+        float lf, mf;
+        const float inv_l = final_scale(a, h, 0.f, -INFINITY, lf, mf);
+        uint16_t* orow = a.o + (((size_t)w.b * a.Hq + h) * a.Sq + pos) * T::D_COLS;
+        store_o_rows_direct<T>(0u, 0u, orow, pos < a.Sq, 0, inv_l, 0, T::D_COLS / 32);
+        if (pos < a.Sq)
+            a.lse[((size_t)w.b * a.Hq + h) * a.Sq + pos] =
+                (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
+    }
+}
+
 // Zeroes rows [r0, 128) of both 64-column chunks of a V slot (all 32 lanes
 // of the calling warp), then makes the writes visible to the tensor core.
 template <class T>
@@ -192,7 +294,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
         if (u >= a.n_full) break;
-        const PrefillWork w = prefill_work<T, T::CAUSAL, false, false>(a, u);
+        const PrefillWork w = wide_work<T>(a, u);
         if (w.n_max <= 0) continue;
         const int plane = w.b * a.Hkv + w.hk;
         // next ring position's slot, once its previous contents were consumed
@@ -251,7 +353,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
             mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
             load_chunks<T, T::NCH>(sQ, tm_q, 0, w.row0, w.b * a.Hq + w.h, bar_q);
             const int un = persist_unit(i + 1, x, G);   // this CTA's next unit
-            if (un < a.n_full) prefetch_q_of<T, T::CAUSAL, false, false>(tm_q, a, un);
+            if (un < a.n_full) wide_prefetch_q<T>(tm_q, a, un);
         }
         __syncwarp();
         ++kq;
@@ -331,7 +433,7 @@ __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem,
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
         if (u >= a.n_full) break;
-        const PrefillWork w = prefill_work<T, T::CAUSAL, false, false>(a, u);
+        const PrefillWork w = wide_work<T>(a, u);
         const int n = w.n_max;
         if (n <= 0) continue;
         if (!mbar_wait_lane(smem_u32(&aux->bar_q), (uint32_t)(kq & 1), wc,
@@ -414,7 +516,11 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
     const int r = (warp & 3) * 32 + lane;                    // row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     int lim = w.L - 1;   // last visible key of this row
-    if (T::CAUSAL) lim = min(lim, w.row0 + r + w.off);
+    if (T::CAUSAL) {
+        int hr, pos;
+        wide_row<T>(a, w, r, hr, pos);
+        lim = min(lim, pos + w.off);
+    }
     const float sl2 = a.scale_log2;
     float m_run = -INFINITY;   // running max of scaled scores, log2 units (the basis)
     float l_run = 0.f;         // this half's running row sum in that basis
@@ -582,28 +688,32 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
         return false;
     tc_fence_after();
     float lf, mf;
-    const float inv_l = final_scale(a, w.h, l, m, lf, mf);
-    const int row = w.row0 + r;
-    const int wrow = w.row0 + (warp & 3) * 32;   // the warp's first row
-    uint16_t* obase = a.o + (((size_t)w.b * a.Hq + w.h) * a.Sq + wrow) * T::D_COLS;
+    int h, row;   // this row's query head and position
+    wide_row<T>(a, w, r, h, row);
+    const float inv_l = final_scale(a, h, l, m, lf, mf);
+    // the warp's first row: its 32 rows are one head's, or (16 positions per
+    // head) two heads', which the O map's box covers
+    int wh, wrow;
+    wide_row<T>(a, w, (warp & 3) * 32, wh, wrow);
+    uint16_t* obase = a.o + (((size_t)w.b * a.Hq + wh) * a.Sq + wrow) * T::D_COLS;
     store_o_rows_staged<T, 2>(lane_base, T::O_COL, obase, T::D_COLS, a.Sq - wrow, n, inv_l, 0,
                               T::D_COLS / 32, stage_of<T>(sQ, warp), tm_o32, 0, wrow,
-                              w.b * a.Hq + w.h);
+                              w.b * a.Hq + wh);
     tc_fence_before();
     mbar_arrive_warp(smem_u32(&aux->bar_odrained));
     if (row < a.Sq)
-        a.lse[((size_t)w.b * a.Hq + w.h) * a.Sq + row] =
+        a.lse[((size_t)w.b * a.Hq + h) * a.Sq + row] =
             (lf > 0.f) ? (mf + lg2_approx(lf)) * kLn2 : -INFINITY;
     return true;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PACK>
 __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
     prefill_kernel_wide(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o32, const PrefillArgs args) {
-    using T = WideTraits<D, CAUSAL>;
+    using T = WideTraits<D, CAUSAL, PACK>;
     static_assert(sizeof(WideAux) <= T::SMEM_AUX, "auxiliary shared block too large");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -652,7 +762,7 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
             if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
-            const PrefillWork w = prefill_work<T, CAUSAL, false, false>(args, u);
+            const PrefillWork w = wide_work<T>(args, u);
             if (w.n_max <= 0) continue;
             if (!wide_softmax_unit<T>(wg, args, w, aux, tmem, wc, J0, kq, tr)) break;
             J0 += w.n_max;
@@ -664,9 +774,9 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
             if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
-            const PrefillWork w = prefill_work<T, CAUSAL, false, false>(args, u);
+            const PrefillWork w = wide_work<T>(args, u);
             if (w.n_max <= 0) {
-                write_empty_unit<T>(args, w);
+                wide_write_empty<T>(args, w);
                 continue;
             }
             if (!wide_correction_unit<T>(&tm_o32, args, w, aux, tmem, sQ, wc, J0, kq)) break;

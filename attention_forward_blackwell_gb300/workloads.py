@@ -90,5 +90,13 @@ DECODE = Workload("decode_gqa_b64_hq64_hkv8_d128", 64, 64, 8, 1, 16384, 128,
                   description="decode GQA B=64 Hq=64 Hkv=8 Sq=1 d=128, "
                               "L_b~U[1024,16384], KV padded to 16384")
 
+# short-query GQA prefill (chunked prefill: 16 new queries per sequence over
+# its cached keys), where the 256-key kernel packs the 8 query heads of a kv
+# group into one tile (not a configuration of the pages)
+CHUNKED_GQA = Workload("chunked_prefill_gqa_b64_hq32_hkv4_q16_k4096_d128", 64, 32, 4, 16, 4096,
+                       128, True, 9,
+                       description="chunked prefill GQA B=64 Hq=32 Hkv=4 Sq=16 Sk=4096 d=128 "
+                                   "causal")
+
 ALL = [TINY, PREFILL_D128, PREFILL_D128_CAUSAL, LONG_D128, LONG_D96, PREFILL_D64, GQA_D256,
-       PREFILL_D512, PREFILL_D512_CAUSAL, DECODE]
+       PREFILL_D512, PREFILL_D512_CAUSAL, DECODE, CHUNKED_GQA]

@@ -88,7 +88,11 @@ typedef enum fa_status {
  * of 128 rows runs instead: one N = 256 score MMA per K-step, P in tensor
  * memory columns of its own, the next block's score MMA issued while the
  * softmax of this one runs, each row's softmax split over two warpgroups
- * (128 keys each) that exchange their block maxima.  For the other
+ * (128 keys each) that exchange their block maxima; with GQA and short
+ * queries (sq <= 64) that kernel packs the query heads of a kv group into
+ * one 128-row tile (P heads x 128 / P positions, P a power of two dividing
+ * hq / hkv: see fa_debug_prefill_plan_gqa), so that they share each K/V tile
+ * ("b200-flash-attention4-planner" E.7, head-packed GQA).  For the other
  * non-causal problems the query blocks of the last, partial wave are split
  * along the key axis over several CTAs and merged on the device (see
  * fa_debug_prefill_plan_ex),
@@ -383,6 +387,22 @@ fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
  */
 fa_status fa_debug_prefill_plan_ex(int batch, int hq, int sq, int sk, int head_dim, int causal,
                                    int window, int paged, int packed, int num_sms, int *out);
+
+/*
+ * fa_debug_prefill_plan_ex with the kv head count: the same plan, with the
+ * 256-key kernel's GQA head packing ("b200-flash-attention4-planner" E.7).
+ * With hq / hkv = G, rows per head R = the next power of two >= sq, at least
+ * 16, at most 128, and P = 128 / R reduced to a power of two dividing G; a
+ * unit is then (batch entry, P consecutive query heads of one kv group,
+ * query block of R positions), its tile row r being head h0 + r / R at
+ * position row0 + r % R.  out: int[7], out[0..5] as fa_debug_prefill_plan_ex
+ * (out[3] = R, the query positions of a unit per head) and out[6] = P, the
+ * query heads per unit (1: no packing).  FA_ERR_INVALID_ARG also when
+ * hkv < 1 or hq is not a multiple of hkv.
+ */
+fa_status fa_debug_prefill_plan_gqa(int batch, int hq, int hkv, int sq, int sk, int head_dim,
+                                    int causal, int window, int paged, int packed, int num_sms,
+                                    int *out);
 
 /* fa_debug_prefill_plan_ex of a dense launch without a window (window = 0,
  * paged = packed = 0), out[0..2] only (out: int[3]). */

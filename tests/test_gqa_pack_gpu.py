@@ -1,0 +1,124 @@
+"""GQA head packing in the 256-key prefill kernel against the fp64 oracle.
+
+With short queries (sq <= 64) and hq / hkv = G > 1, one 128-row tile holds
+P query heads of a kv group x 128 / P query positions, all reading the same
+K/V tiles ("b200-flash-attention4-planner" E.7: explicit head mapping and
+reuse).  These cases cover every P (2, 4, 8) and rows-per-head (16, 32, 64),
+query lengths that fill a head's rows or leave them ragged, the causal mask
+(bottom-right aligned per row position, rows that see no key), per-sequence
+key lengths with NaN padding and empty sequences, attention sinks (a per-row
+head), many units per CTA, and repeated launches.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_parity import THREADS, check_device_error, compare, free_cuda, oracle_for
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from attention_forward_blackwell_gb300 import build
+    build.build()
+    yield
+    free_cuda()
+
+
+def _pack(B, Hq, Hkv, Sq, Sk, d, causal):
+    from attention_forward_blackwell_gb300 import binding
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return binding.debug_prefill_plan_gqa(B, Hq, Hkv, Sq, Sk, d, causal, n_sms).pack
+
+
+CASES = [
+    # B, Hq, Hkv, Sq, Sk, d, lengths, expected heads per tile
+    (2, 8, 1, 1, 700, 128, None, 8),              # 8 heads x 16 rows, one query each
+    (1, 16, 2, 16, 3000, 96, None, 8),            # full 16-row heads
+    (3, 8, 2, 5, 1300, 128, [1300, 0, 257], 4),   # G = 4: 4 heads x 32 rows; an empty sequence
+    (2, 8, 1, 17, 999, 128, [600, 999], 4),       # 17 rows: 32 per head
+    (1, 32, 4, 32, 2048, 128, None, 4),
+    (2, 4, 2, 40, 513, 96, None, 2),              # 64 rows per head, ragged
+    (1, 12, 2, 64, 1500, 128, [1111], 2),         # G = 6: two heads per tile
+    (2, 8, 4, 3, 256, 128, None, 2),              # G = 2
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,lengths,pack", CASES,
+                         ids=[f"b{c[0]}h{c[1]}x{c[2]}q{c[3]}k{c[4]}d{c[5]}" for c in CASES])
+def test_packed_every_element(B, Hq, Hkv, Sq, Sk, d, lengths, pack, causal):
+    from attention_forward_blackwell_gb300 import binding, inputs
+    assert _pack(B, Hq, Hkv, Sq, Sk, d, causal) == pack
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=4100 + Sq + Sk, device="cuda",
+                           lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k)
+    torch.cuda.synchronize()
+    check_device_error()
+    if lengths is not None:
+        for b, L in enumerate(lengths):
+            if L == 0:
+                assert torch.all(o[b] == 0) and torch.all(torch.isneginf(lse[b]))
+    ro, rl = oracle_for(x, scale, causal)
+    compare(o, lse, ro, rl, f"packed {B, Hq, Hkv, Sq, Sk, d} P={pack} causal={causal}")
+    free_cuda()
+
+
+def test_packed_with_sinks():
+    """The sink of each row's own head joins its normaliser."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    B, Hq, Hkv, Sq, Sk, d = 2, 16, 2, 12, 2500, 128
+    assert _pack(B, Hq, Hkv, Sq, Sk, d, True) == 8
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=4200, device="cuda")
+    g = torch.Generator().manual_seed(23)
+    sinks = (2.0 * torch.randn(Hq, generator=g)).float().cuda()
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal, sinks=sinks)
+        torch.cuda.synchronize()
+        check_device_error()
+        ro, rl = oracle.attention_fwd(inputs.bf16_bits(x.q), inputs.bf16_bits(x.k),
+                                      inputs.bf16_bits(x.v), scale=scale, causal=causal,
+                                      threads=THREADS, sinks=sinks.cpu().double().numpy())
+        compare(o, lse, ro, rl, f"packed with sinks causal={causal}")
+    free_cuda()
+
+
+def test_packed_many_units_and_repeats():
+    """A chunked-prefill shape: 64 sequences x 4 kv groups of 8 heads, 16 new
+    queries each over 4,096 keys -- 256 packed units (2,048 unpacked) walked
+    by the persistent CTAs; sampled rows against the oracle, then bit-equal
+    results over repeated launches."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    B, Hq, Hkv, Sq, Sk, d = 64, 32, 4, 16, 4096, 128
+    assert _pack(B, Hq, Hkv, Sq, Sk, d, True) == 8
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=4300, device="cuda",
+                           lengths=(1, Sk))
+    inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+    inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.prefill(x.q, x.k, x.v, scale=scale, causal=True, seqlens_k=x.seqlens_k)
+    torch.cuda.synchronize()
+    check_device_error()
+    rng = np.random.default_rng(5)
+    total = B * Hq * Sq
+    rows = np.unique(np.concatenate([np.arange(0, 2 * Hq * Sq), rng.integers(0, total, 1500),
+                                     np.arange(total - Hq * Sq, total)]))
+    ro, rl = oracle_for(x, scale, True, rows=rows)
+    idx = torch.from_numpy(rows).cuda()
+    compare(o.view(-1, d)[idx], lse.view(-1)[idx], ro, rl, "packed chunked prefill (sampled)")
+    for _ in range(3):
+        o2, l2 = binding.prefill(x.q, x.k, x.v, scale=scale, causal=True,
+                                 seqlens_k=x.seqlens_k)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o2) and torch.equal(lse, l2)
+    check_device_error()
+    free_cuda()

@@ -104,3 +104,45 @@ def test_plan_rejects_bad_sizes():
         binding.debug_prefill_plan(1, 1, 128, 128, 128, False, 0)
     with pytest.raises(binding.FaError):
         binding.debug_prefill_plan_ex(1, 1, 128, 128, 128, False, 0, paged=True)
+
+
+@pytest.mark.parametrize("sq", [1, 7, 16, 17, 32, 33, 64, 65, 128, 4096])
+@pytest.mark.parametrize("hq,hkv", [(32, 4), (16, 8), (12, 2), (8, 8), (6, 1), (4, 1)])
+@pytest.mark.parametrize("d,kind", [(128, (0, False, False)), (96, (0, False, False)),
+                                    (64, (0, False, False)), (128, (64, False, False)),
+                                    (128, (0, True, False))])
+def test_gqa_head_packing_plan(sq, hq, hkv, d, kind):
+    """Query heads per unit of the 256-key kernel: rows per head R = the next
+    power of two >= sq in [16, 128], P = 128 / R reduced to a power of two
+    dividing hq / hkv; units = batch x hq / P x ceil(sq / R).  Other kernels
+    (head_dim 64, windows, paged caches) never pack."""
+    window, paged, packed = kind
+    batch, sk = 3, 1000
+    p = binding.debug_prefill_plan_gqa(batch, hq, hkv, sq, sk, d, False, 152, window=window,
+                                       paged=paged, packed=packed)
+    g = hq // hkv
+    if not _wide(d, False, window, paged, packed):
+        assert p.pack == 1
+        return
+    rows = 16
+    while rows < sq and rows < 128:
+        rows *= 2
+    pack = 128 // rows
+    while pack > 1 and g % pack:
+        pack //= 2
+    assert p.pack == pack
+    assert p.rows_per_unit == 128 // pack
+    assert p.n_full == batch * (hq // pack) * math.ceil(sq / p.rows_per_unit)
+    assert (p.n_tail, p.split, p.keys_per_block, p.persistent) == (0, 1, 256, True)
+    # without the kv head count (or with hkv = hq) nothing is packed
+    assert tuple(binding.debug_prefill_plan_ex(batch, hq, sq, sk, d, False, 152, window=window,
+                                               paged=paged, packed=packed)) == \
+        tuple(binding.debug_prefill_plan_gqa(batch, hq, hq, sq, sk, d, False, 152,
+                                             window=window, paged=paged, packed=packed))[:6]
+
+
+def test_gqa_plan_rejects_bad_group():
+    with pytest.raises(binding.FaError):
+        binding.debug_prefill_plan_gqa(1, 6, 4, 16, 128, 128, False, 152)
+    with pytest.raises(binding.FaError):
+        binding.debug_prefill_plan_gqa(1, 6, 0, 16, 128, 128, False, 152)
