@@ -63,12 +63,12 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("943cb0505a85c241125551eb78df1728c356549e2c887990598d1ece054ff8e2",
-                "long_prefill_b1_h16_s8192_d128", 115654400),
-    # captured at batch 16 (463.78 MB, 1.017 x its algorithmic bytes) and
+    "prefill": ("ed8a858fdd4f4a1e7517b6b1b935445e69996749c6f4db5a6c067e6dc34057b6",
+                "long_prefill_b1_h16_s8192_d128", 115893504),
+    # captured at batch 16 (463.66 MB, 1.017 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
-    "decode": ("b3d5f849c25e7011fb921fdf56efe964d17581b057432e737006646007fd9890",
-               "decode_gqa_b64_hq64_hkv8_d128", 2206020388),
+    "decode": ("6ff7d2c6ac0365ca5fd8b80ea2e46d75363b1b86b70345db738ab9a9aead4b3f",
+               "decode_gqa_b64_hq64_hkv8_d128", 2205418853),
 }
 
 
