@@ -202,6 +202,22 @@ fa_status check_paged(const int* seqlens_k, const int* block_table, int max_page
     return FA_OK;
 }
 
+struct Varlen;
+fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
+                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
+                       float scale, int causal, int window, const float* sinks,
+                       const int* block_table, int max_pages, int page_size, int num_pages,
+                       fa_stream_t stream, const Varlen* vl);
+
+// Query rows per kv head (G * sq) from which a decode call at head_dim 128
+// runs the head-packed prefill kernel instead of the split-KV kernel.
+// Measured on GB300 (B=64, Hq=64, Hkv=8, key lengths 1K-16K): the split-KV
+// kernel 6497 / 6353 / 5169 / 3086 / 1707 GB/s at sq = 1 / 2 / 4 / 8 / 16,
+// the packed prefill kernel 5169-5244 GB/s throughout; with G = 4, sq = 8
+// (32 rows) 2853 against 4631.  Past 16 rows the split kernel's query tiles
+// (16 rows each on mma.sync) make it compute-bound.
+constexpr int kDecodeToPrefillRows = 32;
+
 fa_status decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
                       float scale, int causal, int window, const float* sinks, int num_splits,
@@ -223,6 +239,13 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
         return from_cuda(launch_fill_empty(static_cast<uint16_t*>(o), lse,
                                            (long long)batch * hq * sq, head_dim, sinks, hq, sq,
                                            s));
+    // several queries of a GQA group (contiguous caches, no window, the
+    // library's own split count): the prefill kernel with the group's heads
+    // packed into one tile
+    if (num_splits <= 0 && block_table == nullptr && window <= 0 && head_dim == 128 &&
+        (hq / hkv) * sq >= kDecodeToPrefillRows)
+        return prefill_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
+                            causal, 0, sinks, nullptr, 0, 0, 0, stream, nullptr);
 
     DecodeArgs a{};
     a.q = static_cast<const uint16_t*>(q);

@@ -45,6 +45,10 @@ CASES = [
     (2, 4, 2, 40, 513, 96, None, 2),              # 64 rows per head, ragged
     (1, 12, 2, 64, 1500, 128, [1111], 2),         # G = 6: two heads per tile
     (2, 8, 4, 3, 256, 128, None, 2),              # G = 2
+    (1, 8, 1, 1, 1, 128, None, 8),                # one key
+    (2, 16, 2, 64, 64, 96, None, 2),              # short square: the causal triangle
+    (1, 8, 1, 16, 257, 128, [257], 8),            # a last key block of one key
+    (2, 8, 2, 30, 20, 128, [20, 7], 4),           # Sq > Sk: causal rows without keys
 ]
 
 
@@ -121,4 +125,54 @@ def test_packed_many_units_and_repeats():
         torch.cuda.synchronize()
         assert torch.equal(o, o2) and torch.equal(lse, l2)
     check_device_error()
+    free_cuda()
+
+
+DECODE_ROUTED = [
+    # B, Hq, Hkv, Sq, Sk, lengths, causal, sinks: (Hq / Hkv) * Sq >= 32 rows
+    (8, 32, 4, 4, 3000, (1, 3000), True, False),
+    (4, 64, 8, 16, 2048, None, False, True),
+    (6, 16, 2, 16, 5000, [5000, 0, 1, 4999, 2500, 17], True, True),
+    (3, 32, 2, 2, 700, None, False, False),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,lengths,causal,sinks_on", DECODE_ROUTED,
+                         ids=[f"b{c[0]}h{c[1]}x{c[2]}q{c[3]}k{c[4]}" for c in DECODE_ROUTED])
+def test_decode_with_many_rows_per_kv_head_runs_the_packed_kernel(B, Hq, Hkv, Sq, Sk, lengths,
+                                                                   causal, sinks_on):
+    """fa_fwd_decode / fa_fwd_decode_ex at head_dim 128 with >= 32 query rows
+    per kv head give fa_fwd_prefill's result bit for bit (the same packed
+    kernel ran) and match the oracle on every element."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    d = 128
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=4400 + Sq + Sk, device="cuda",
+                           lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    sinks = None
+    if sinks_on:
+        g = torch.Generator().manual_seed(Sq + Sk)
+        sinks = (2.0 * torch.randn(Hq, generator=g)).float().cuda()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = binding.decode(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k,
+                            sinks=sinks)
+    o2, l2 = binding.prefill(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k,
+                             sinks=sinks)
+    torch.cuda.synchronize()
+    check_device_error()
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    lens = None if x.seqlens_k is None else x.seqlens_k.cpu().tolist()
+    ro, rl = oracle.attention_fwd(inputs.bf16_bits(x.q), inputs.bf16_bits(x.k),
+                                  inputs.bf16_bits(x.v), scale=scale, causal=causal,
+                                  seqlens_k=lens, threads=THREADS,
+                                  sinks=None if sinks is None else sinks.cpu().double().numpy())
+    compare(o, lse, ro, rl, f"decode routed {B, Hq, Hkv, Sq, Sk} causal={causal} sinks={sinks_on}")
+    # an explicit split count keeps the split-KV kernel (same values within
+    # the parity tolerance, not the same bits)
+    o3, l3 = binding.decode(x.q, x.k, x.v, scale=scale, causal=causal, seqlens_k=x.seqlens_k,
+                            num_splits=3) if sinks is None else (o, lse)
+    torch.cuda.synchronize()
+    compare(o3, l3, ro, rl, "decode with 3 splits")
     free_cuda()
