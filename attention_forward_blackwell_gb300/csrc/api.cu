@@ -209,14 +209,19 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
                        const int* block_table, int max_pages, int page_size, int num_pages,
                        fa_stream_t stream, const Varlen* vl);
 
-// Query rows per kv head (G * sq) from which a decode call at head_dim 128
-// runs the head-packed prefill kernel instead of the split-KV kernel.
-// Measured on GB300 (B=64, Hq=64, Hkv=8, key lengths 1K-16K): the split-KV
-// kernel 6497 / 6353 / 5169 / 3086 / 1707 GB/s at sq = 1 / 2 / 4 / 8 / 16,
-// the packed prefill kernel 5169-5244 GB/s throughout; with G = 4, sq = 8
-// (32 rows) 2853 against 4631.  Past 16 rows the split kernel's query tiles
-// (16 rows each on mma.sync) make it compute-bound.
+// When a decode call at head_dim 128 runs the head-packed prefill kernel
+// instead of the split-KV kernel: at least kDecodeToPrefillRows query rows
+// per kv head (G * sq), and the packed launch's units x those rows at least
+// kDecodeToPrefillWork.  Past 16 rows per kv head the split kernel's query
+// tiles (16 rows each on mma.sync) make it compute-bound (B=64, Hq=64,
+// Hkv=8, key lengths 1K-16K: 6497 / 6353 / 5169 / 3086 / 1707 GB/s at
+// sq = 1 / 2 / 4 / 8 / 16, the packed kernel 5169-5244 throughout); but the
+// packed kernel never splits a unit along the keys, so with few units it
+// takes one unit's time on few SMs.  Measured at 16K keys, split time over
+// packed time: 32 rows x 8 / 16 / 32 units 0.64 / 1.02 / 1.41; 64 rows x
+// 8 / 16 units 0.91-0.95 / 1.37; 128 rows x 4 / 8 units 0.89 / 1.35.
 constexpr int kDecodeToPrefillRows = 32;
+constexpr long long kDecodeToPrefillWork = 1024;
 
 fa_status decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
@@ -242,8 +247,11 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     // several queries of a GQA group (contiguous caches, no window, the
     // library's own split count): the prefill kernel with the group's heads
     // packed into one tile
+    const int rows_per_kv = (hq / hkv) * sq;
     if (num_splits <= 0 && block_table == nullptr && window <= 0 && head_dim == 128 &&
-        (hq / hkv) * sq >= kDecodeToPrefillRows)
+        rows_per_kv >= kDecodeToPrefillRows &&
+        prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, 0, false, false, di->num_sms,
+                      hq / hkv).units * rows_per_kv >= kDecodeToPrefillWork)
         return prefill_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
                             causal, 0, sinks, nullptr, 0, 0, 0, stream, nullptr);
 

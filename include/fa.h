@@ -140,13 +140,16 @@ fa_status fa_fwd_prefill_ex(const void *q, const void *k, const void *v, void *o
  * Same arguments as fa_fwd_prefill; sq must be 1..FA_DECODE_MAX_SQ and
  * head_dim one of 64, 128, 256.  The partials live in a workspace that the
  * call allocates and frees stream-ordered (cudaMallocAsync/cudaFreeAsync on
- * `stream`).  At head_dim 128 with (hq / hkv) * sq >= 32 query rows per
- * key/value head (several queries of a GQA group), this call and
+ * `stream`).  At head_dim 128 with R = (hq / hkv) * sq >= 32 query rows per
+ * key/value head (several queries of a GQA group) and enough of them
+ * (U * R >= 1024, U the units of the packed launch as
+ * fa_debug_prefill_plan_gqa reports them in out[0]), this call and
  * fa_fwd_decode_ex without a window run the prefill kernel with the group's
  * query heads packed into one tile instead (the same result as
  * fa_fwd_prefill / fa_fwd_prefill_ex, bit for bit; no workspace): past 16
  * rows per key/value head the split kernel is bound by its tensor-core
- * work, the packed kernel by HBM.  fa_fwd_decode_splits, the paged and the
+ * work, the packed kernel by HBM, as long as its units (never split along
+ * the keys) fill the GPU.  fa_fwd_decode_splits, the paged and the
  * no-allocation entry points always run the split kernel.
  */
 fa_status fa_fwd_decode(const void *q, const void *k, const void *v, void *o,

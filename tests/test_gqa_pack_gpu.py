@@ -129,12 +129,21 @@ def test_packed_many_units_and_repeats():
 
 
 DECODE_ROUTED = [
-    # B, Hq, Hkv, Sq, Sk, lengths, causal, sinks: (Hq / Hkv) * Sq >= 32 rows
-    (8, 32, 4, 4, 3000, (1, 3000), True, False),
-    (4, 64, 8, 16, 2048, None, False, True),
-    (6, 16, 2, 16, 5000, [5000, 0, 1, 4999, 2500, 17], True, True),
-    (3, 32, 2, 2, 700, None, False, False),
+    # B, Hq, Hkv, Sq, Sk, lengths, causal, sinks: R = (Hq / Hkv) * Sq >= 32
+    # rows per kv head and packed units x R >= 1024
+    (8, 32, 4, 4, 3000, (1, 3000), True, False),        # 32 units x 32 rows
+    (4, 64, 8, 16, 2048, None, False, True),            # 32 x 128
+    (6, 16, 2, 16, 5000, [5000, 0, 1, 4999, 2500, 17], True, True),   # 12 x 128
+    (12, 32, 2, 2, 700, None, False, False),            # G = 16: 48 x 32
 ]
+
+
+def _routed(B, Hq, Hkv, Sq, Sk, causal):
+    from attention_forward_blackwell_gb300 import binding
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = Hq // Hkv * Sq
+    units = binding.debug_prefill_plan_gqa(B, Hq, Hkv, Sq, Sk, 128, causal, n_sms).n_full
+    return rows >= 32 and units * rows >= 1024
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,lengths,causal,sinks_on", DECODE_ROUTED,
@@ -146,6 +155,7 @@ def test_decode_with_many_rows_per_kv_head_runs_the_packed_kernel(B, Hq, Hkv, Sq
     kernel ran) and match the oracle on every element."""
     from attention_forward_blackwell_gb300 import binding, inputs
     d = 128
+    assert _routed(B, Hq, Hkv, Sq, Sk, causal)
     x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=4400 + Sq + Sk, device="cuda",
                            lengths=lengths)
     if lengths is not None:
