@@ -43,6 +43,12 @@ def prefill_flops(B, Hq, Sq, Sk, d, causal):
     return f * 0.5 if causal else f
 
 
+def prefill_bytes(B, Hq, Hkv, Sq, Sk, d):
+    """Algorithmic HBM bytes of one prefill pass without key lengths: K and V
+    once per kv head, Q and O once (bf16), LSE (fp32)."""
+    return 2 * B * Hkv * Sk * d * 2 + 2 * B * Hq * Sq * d * 2 + B * Hq * Sq * 4
+
+
 def decode_bytes(Hkv, Hq, d, lengths, Sq=1):
     """Algorithmic HBM bytes of one decode pass (bf16 K/V/Q/O, fp32 LSE)."""
     B = len(lengths)

@@ -269,7 +269,7 @@ def bench_workloads(decode_batch=None):
     return [("long_d128", W.LONG_D128), ("d128", W.PREFILL_D128),
             ("d128_causal", W.PREFILL_D128_CAUSAL), ("d96", W.LONG_D96),
             ("gqa_d256_causal", W.GQA_D256), ("d64", W.PREFILL_D64), ("tiny_d64", W.TINY),
-            ("decode", dec)]
+            ("chunked_gqa", W.CHUNKED_GQA), ("decode", dec)]
 
 
 class Case:
@@ -315,6 +315,11 @@ class Case:
 def W_prefill_flops(w):
     from attention_forward_blackwell_gb300 import workloads as W
     return W.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.d, w.causal)
+
+
+def W_prefill_bytes(w):
+    from attention_forward_blackwell_gb300 import workloads as W
+    return W.prefill_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d)
 
 
 def W_decode_bytes(w, lens):
@@ -388,6 +393,16 @@ def run_ours(args, dist):
             if key == "tiny_d64":
                 e["us"] = round(med * 1e3, 2)
                 e["note"] = "latency-bound (4.19 MFLOP): the roofline fraction does not apply"
+            if key == "chunked_gqa":
+                # 16 queries per sequence: 128 FLOP per K/V byte, HBM-bound;
+                # the causal-halved FLOP count undercounts (the mask removes
+                # almost nothing of 4,096 keys)
+                nbytes = W_prefill_bytes(w)
+                gbs = aggregate(nbytes / dist.world, dist.world, med * 1e-3) / 1e9
+                e.update({"GB_per_s": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                          "algorithmic_bytes": nbytes, "bound": "hbm",
+                          "note": "GQA head packing: the 8 query heads of a kv group share "
+                                  "one 128-row tile"})
         breakdown[key] = e
 
     head_key, head = cases[0]

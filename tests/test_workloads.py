@@ -43,3 +43,14 @@ def test_workload_shapes_match_configuration():
     assert (w.GQA_D256.Hq // w.GQA_D256.Hkv, w.GQA_D256.k_scale) == (8, 0.5)
     assert w.DECODE.lengths == (1024, 16384) and w.DECODE.Sk == 16384
     assert abs(w.PREFILL_D128.scale - 128 ** -0.5) < 1e-15
+
+
+def test_prefill_bytes_counts_each_tensor_once():
+    """K and V once per kv head (not per query head), Q and O in bf16, LSE fp32:
+    the chunked GQA workload's 8 query heads per kv head add no K/V bytes."""
+    w = workloads.CHUNKED_GQA
+    kv = 2 * w.B * w.Hkv * w.Sk * w.d * 2
+    qo = 2 * w.B * w.Hq * w.Sq * w.d * 2
+    assert workloads.prefill_bytes(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d) == \
+        kv + qo + w.B * w.Hq * w.Sq * 4
+    assert workloads.prefill_bytes(1, 8, 1, 1, 100, 64) < workloads.prefill_bytes(1, 8, 8, 1, 100, 64)
