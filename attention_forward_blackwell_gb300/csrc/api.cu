@@ -209,19 +209,15 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
                        const int* block_table, int max_pages, int page_size, int num_pages,
                        fa_stream_t stream, const Varlen* vl);
 
-// When a decode call at head_dim 128 runs the head-packed prefill kernel
-// instead of the split-KV kernel: at least kDecodeToPrefillRows query rows
-// per kv head (G * sq), and the packed launch's units x those rows at least
-// kDecodeToPrefillWork.  Past 16 rows per kv head the split kernel's query
-// tiles (16 rows each on mma.sync) make it compute-bound (B=64, Hq=64,
-// Hkv=8, key lengths 1K-16K: 6497 / 6353 / 5169 / 3086 / 1707 GB/s at
-// sq = 1 / 2 / 4 / 8 / 16, the packed kernel 5169-5244 throughout); but the
-// packed kernel never splits a unit along the keys, so with few units it
-// takes one unit's time on few SMs.  Measured at 16K keys, split time over
-// packed time: 32 rows x 8 / 16 / 32 units 0.64 / 1.02 / 1.41; 64 rows x
-// 8 / 16 units 0.91-0.95 / 1.37; 128 rows x 4 / 8 units 0.89 / 1.35.
+// Query rows per kv head (G * sq) from which a decode call at head_dim 128
+// runs the head-packed prefill kernel instead of the split-KV kernel.  Past
+// 16 rows per kv head the split kernel's query tiles (16 rows each on
+// mma.sync) make it compute-bound (B=64, Hq=64, Hkv=8, key lengths 1K-16K:
+// 6497 / 6353 / 5169 / 3086 / 1707 GB/s at sq = 1 / 2 / 4 / 8 / 16, the
+// packed kernel 5169-5244 throughout); with few units the packed kernel
+// splits them along the keys over the idle SMs, so that at 16K keys it is
+// 1.2-3.9x faster for every batch from 1 to 16 at 32 to 128 rows.
 constexpr int kDecodeToPrefillRows = 32;
-constexpr long long kDecodeToPrefillWork = 1024;
 
 fa_status decode_impl(const void* q, const void* k, const void* v, void* o, float* lse, int batch,
                       int hq, int hkv, int sq, int sk, const int* seqlens_k, int head_dim,
@@ -247,11 +243,8 @@ fa_status decode_impl(const void* q, const void* k, const void* v, void* o, floa
     // several queries of a GQA group (contiguous caches, no window, the
     // library's own split count): the prefill kernel with the group's heads
     // packed into one tile
-    const int rows_per_kv = (hq / hkv) * sq;
     if (num_splits <= 0 && block_table == nullptr && window <= 0 && head_dim == 128 &&
-        rows_per_kv >= kDecodeToPrefillRows &&
-        prefill_shape(batch, hq, sq, sk, head_dim, causal != 0, 0, false, false, di->num_sms,
-                      hq / hkv).units * rows_per_kv >= kDecodeToPrefillWork)
+        (hq / hkv) * sq >= kDecodeToPrefillRows)
         return prefill_impl(q, k, v, o, lse, batch, hq, hkv, sq, sk, seqlens_k, head_dim, scale,
                             causal, 0, sinks, nullptr, 0, 0, 0, stream, nullptr);
 
@@ -441,10 +434,11 @@ fa_status prefill_impl(const void* q, const void* k, const void* v, void* o, flo
     const PrefillPlan plan = shape.plan;
     a.n_full = plan.n_full;
     a.split = plan.split;
+    a.n_work = plan.n_full + plan.n_tail * plan.split;
     p.n_tail = plan.n_tail;
     void* ws = nullptr;
     if (plan.n_tail > 0) {
-        const int nq = shape.rows_per_unit / 128;
+        const int nq = wide ? 1 : shape.rows_per_unit / 128;   // Q tiles of a unit
         const size_t pieces = (size_t)plan.n_tail * plan.split;
         const size_t part_o = pieces * nq * head_dim * 128 * sizeof(float);
         const size_t part_ml = pieces * nq * 2 * 128 * sizeof(float);

@@ -55,6 +55,7 @@ struct PrefillArgs {
     // each later unit is split into `split` pieces of its nk key blocks.
     int n_full;
     int split;
+    int n_work;                 // work items of a persistent launch: n_full + n_tail * split
     int nk;                     // key blocks of a unit, ceil(Sk / keys per block)
     // Scratch of the split units (nullptr when nothing is split): partial O
     // of every piece, [pieces][NQ][d / 4][128][4] fp32, its row max and row
@@ -184,9 +185,19 @@ inline PrefillShape prefill_shape(int batch, int hq, int sq, int sk, int head_di
     s.nk = (sk + s.keys_per_block - 1) / s.keys_per_block;
     // not split: causal units (heaviest first), windowed ones (fewer key
     // blocks than nk), packed sequences (units of different lengths), head_dim
-    // 512 (two CTAs per unit already), the persistent 256-key kernel
+    // 512 (two CTAs per unit already)
     s.plan = plan_prefill(s.units, s.nk,
                           causal || window > 0 || packed || head_dim == 512 || s.wide, num_sms);
+    // the 256-key kernel with at most half a wave of (non-causal) units: each
+    // unit in `split` pieces of >= 4 key blocks, one piece per CTA, so that
+    // the SMs the units leave idle share the keys (the last piece to finish
+    // merges); with more units it walks them whole
+    if (s.wide && !causal && s.units > 0 && s.units * 2 <= num_sms) {
+        long long k = num_sms / s.units;
+        if (k > 8) k = 8;
+        if (k > s.nk / 4) k = s.nk / 4;
+        if (k >= 2) s.plan = PrefillPlan{0, (int)s.units, (int)k};
+    }
     // head_dim 256 launches of whole units, and the 256-key kernel, run one
     // persistent CTA per SM
     s.persistent = s.wide || (head_dim == 256 && !packed && s.plan.n_tail == 0 &&

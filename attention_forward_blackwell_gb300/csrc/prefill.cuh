@@ -1412,8 +1412,8 @@ __device__ __forceinline__ void store_o32(uint16_t* orow, const float (&v)[32], 
 // unit's counter, and the one that arrives last sets aux->merge_last; its CTA
 // then merges the unit at the end of the kernel (merge_unit, all threads).
 // No CTA waits for another.
-template <class T>
-__device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, PrefillAux<T>* aux,
+template <class T, class Aux>
+__device__ void split_arrive(const PrefillArgs& a, const PrefillWork& w, Aux* aux,
                              const WaitCtx& wc) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     mbar_arrive_warp(smem_u32(&aux->bar_split_a));   // this warp's stores issued
@@ -1464,14 +1464,18 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
                            int nthr) {
     constexpr int NC16 = T::D_COLS / 16;
     const int s0 = tail * a.split;
-    const float sg = (a.sinks != nullptr) ? a.sinks[h] * kLog2e : -INFINITY;
+    // head-packed tiles (a.pack > 1): row r is head h + r / R at position
+    // row0 + r % R, R = BM / pack
+    const int prows = T::BM / (a.pack > 1 ? a.pack : 1);
 #pragma unroll 1
     for (int task = tid; task < T::NQ * NC16 * T::BM; task += nthr) {
         const int r = task % T::BM;
         const int c16 = (task / T::BM) % NC16;
         const int t = task / (T::BM * NC16);
-        const int row = row0 + t * T::BM + r;
+        const int hr = a.pack > 1 ? h + r / prows : h;
+        const int row = a.pack > 1 ? row0 + r % prows : row0 + t * T::BM + r;
         if (row >= a.Sq) continue;
+        const float sg = (a.sinks != nullptr) ? a.sinks[hr] * kLog2e : -INFINITY;
         float M = sg;
         float L = (sg == -INFINITY) ? 0.f : 1.f;
         float acc[16];
@@ -1503,7 +1507,7 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
         }
         const float inv_l = (L > 0.f) ? 1.f / L : 0.f;
         uint4* dst = reinterpret_cast<uint4*>(
-            a.o + (((size_t)b * a.Hq + h) * a.Sq + row) * T::D_COLS + c16 * 16);
+            a.o + (((size_t)b * a.Hq + hr) * a.Sq + row) * T::D_COLS + c16 * 16);
 #pragma unroll
         for (int g8 = 0; g8 < 2; ++g8) {
             uint4 v;
@@ -1514,7 +1518,7 @@ __device__ void merge_unit(const PrefillArgs& a, int tail, int h, int b, int row
             dst[g8] = v;
         }
         if (c16 == 0)
-            a.lse[((size_t)b * a.Hq + h) * a.Sq + row] =
+            a.lse[((size_t)b * a.Hq + hr) * a.Sq + row] =
                 (L > 0.f) ? (M + lg2_approx(L)) * kLn2 : -INFINITY;
     }
 }
@@ -2172,17 +2176,21 @@ cudaError_t launch_prefill_impl(const PrefillLaunch& p, cudaStream_t stream) {
         // dense, no window: 256-key score blocks, one persistent CTA per SM
         if (p.wide) {
             using W = WideTraits<D>;
-            // (head-packed GQA tiles: an instance of their own)
+            // (head-packed GQA tiles, and units split along the keys: instances
+            // of their own; split launches are never causal)
+            const bool split = p.n_tail > 0;
             const PrefillKernelFn kern =
-                p.args.pack > 1
-                    ? (p.causal ? prefill_kernel_wide<D, true, true>
-                                : prefill_kernel_wide<D, false, true>)
-                    : (p.causal ? prefill_kernel_wide<D, true, false>
-                                : prefill_kernel_wide<D, false, false>);
+                split ? (p.args.pack > 1 ? prefill_kernel_wide<D, false, true, true>
+                                         : prefill_kernel_wide<D, false, false, true>)
+                : p.args.pack > 1
+                    ? (p.causal ? prefill_kernel_wide<D, true, true, false>
+                                : prefill_kernel_wide<D, false, true, false>)
+                    : (p.causal ? prefill_kernel_wide<D, true, false, false>
+                                : prefill_kernel_wide<D, false, false, false>);
             cudaError_t e = cudaFuncSetAttribute(
                 kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W::SMEM_TOTAL);
             if (e != cudaSuccess) return e;
-            const unsigned grid = (unsigned)min(p.args.n_full, p.num_sms);
+            const unsigned grid = (unsigned)min(p.args.n_work, p.num_sms);
             kern<<<grid, W::THREADS, W::SMEM_TOTAL, stream>>>(p.tm_q, p.tm_k, p.tm_v, p.tm_o32,
                                                               p.args);
             return cudaGetLastError();

@@ -91,10 +91,11 @@ namespace fa {
 
 constexpr int kWideSlots = 5;   // ring slots of the 256-key kernel
 
-template <int D, bool C = false, bool PK = false>
+template <int D, bool C = false, bool PK = false, bool SP = false>
 struct WideTraits {
     static constexpr bool CAUSAL = C;               // causal mask (bottom-right aligned)
     static constexpr bool PACK = PK;                // GQA head packing (PrefillArgs::pack > 1)
+    static constexpr bool SPLIT = SP;               // units split along the keys, one piece per CTA
     static constexpr int BM = 128;                  // query rows of a unit = TMEM lanes
     static constexpr int BN = 256;                  // keys per score block
     static constexpr int NQ = 1;                    // (shared work split: one Q tile)
@@ -158,11 +159,25 @@ struct WideAux {
     uint64_t bar_odrained;
     uint64_t bar_tail;
     uint64_t bar_drain;
+    uint64_t bar_split_a;     // a piece's partial result written (4 correction warps)
     uint32_t tmem_base;
     int abort_flag;
+    int merge_last;           // this CTA's piece arrived last: it merges the unit
+    int merge_unit[4];        // tail, head, batch entry, first row of that unit
     float xm[2][2][128];      // [J & 1][half][row] block maxima
     float mb_l[2][128];       // [half][row] row sums of the unit
 };
+
+// Work items of a launch: whole units only (n_full), or (SPLIT instances)
+// pieces as well.  The bound is n_full unless the instance splits, so that
+// the compiler sees every item as a whole unit and drops prefill_work's piece
+// arithmetic from the roles (measured on GB300: bounding the unsplit
+// kernels' loops by n_work instead, the same value at run time, made them
+// 10 % slower).
+template <class T>
+__device__ __forceinline__ int wide_items(const PrefillArgs& a) {
+    return T::SPLIT ? a.n_work : a.n_full;
+}
 
 // Unit u of the 256-key kernel.  Without packing, prefill_work's unit
 // (batch entry, query head, block of 128 query rows).  With P = a.pack heads
@@ -176,6 +191,18 @@ __device__ __forceinline__ PrefillWork wide_work(const PrefillArgs& a, int u) {
         return prefill_work<T, T::CAUSAL, false, false>(a, u);
     } else {
         PrefillWork w;
+        int kb = 0, ke = 0x7fffffff;   // key blocks [kb, ke) of a piece
+        w.piece = -1;
+        w.tail = -1;
+        if (u >= a.n_full) {   // piece k of split unit `tail`, as prefill_work cuts them
+            const int q = u - a.n_full;
+            const int k = q % a.split;
+            w.tail = q / a.split;
+            w.piece = q;
+            kb = (int)((long long)k * a.nk / a.split);
+            ke = (int)((long long)(k + 1) * a.nk / a.split);
+            u = a.n_full + w.tail;
+        }
         const int rows = T::BM / a.pack;            // query positions per head
         const int ng = a.Hq / a.pack;               // head groups per batch entry
         const int nbh = a.B * ng;
@@ -193,11 +220,10 @@ __device__ __forceinline__ PrefillWork wide_work(const PrefillArgs& a, int u) {
         int last = L - 1;   // last key any row of the tile can see
         if (T::CAUSAL) last = min(last, w.row0 + rows - 1 + w.off);
         const int n = last >= 0 ? last / T::BN + 1 : 0;
-        w.kb = 0;
-        w.n_kv[0] = w.n_kv[1] = n;
-        w.n_max = n;
-        w.piece = -1;
-        w.tail = -1;
+        const int cnt = min(n, ke) - kb;
+        w.kb = kb;
+        w.n_kv[0] = w.n_kv[1] = cnt > 0 ? cnt : 0;
+        w.n_max = w.n_kv[0];
         w.Lq = w.q0 = w.k0 = 0;
         w.dv0 = 0;
         return w;
@@ -293,7 +319,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     bool ok = true;
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
-        if (u >= a.n_full) break;
+        if (u >= wide_items<T>(a)) break;
         const PrefillWork w = wide_work<T>(a, u);
         if (w.n_max <= 0) continue;
         const int plane = w.b * a.Hkv + w.hk;
@@ -353,7 +379,7 @@ __device__ void wide_load_role(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
             mbar_arrive_expect_tx(bar_q, (uint32_t)T::QTILE);
             load_chunks<T, T::NCH>(sQ, tm_q, 0, w.row0, w.b * a.Hq + w.h, bar_q);
             const int un = persist_unit(i + 1, x, G);   // this CTA's next unit
-            if (un < a.n_full) wide_prefetch_q<T>(tm_q, a, un);
+            if (un < wide_items<T>(a)) wide_prefetch_q<T>(tm_q, a, un);
         }
         __syncwarp();
         ++kq;
@@ -432,7 +458,7 @@ __device__ void wide_mma_role(const PrefillArgs& a, WideAux* aux, uint32_t tmem,
     bool ok = true;
     for (int i = 0; ok; ++i) {
         const int u = persist_unit(i, x, G);
-        if (u >= a.n_full) break;
+        if (u >= wide_items<T>(a)) break;
         const PrefillWork w = wide_work<T>(a, u);
         const int n = w.n_max;
         if (n <= 0) continue;
@@ -545,7 +571,7 @@ __device__ bool wide_softmax_unit(int h, const PrefillArgs& a, const PrefillWork
         float s[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(u[c >> 5][c & 31]);
-        const int kv0 = j * T::BN + h * 128;   // first key of the half, from the piece's start
+        const int kv0 = (w.kb + j) * T::BN + h * 128;   // first key of the half
         if (lim - kv0 < 127) {
             const int nvis = lim - kv0 + 1;
 #pragma unroll
@@ -687,6 +713,33 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
                    kErrWaitTimeout | kSiteEpiPv))
         return false;
     tc_fence_after();
+    if constexpr (T::SPLIT) {
+        if (w.piece >= 0) {
+            // a piece of a split unit: unnormalised O (in the basis m), m
+            // and l -> the piece's scratch slot; the last piece to arrive
+            // merges the unit at the kernel's end
+            float4* po = reinterpret_cast<float4*>(a.part_o +
+                                                   (size_t)w.piece * (T::D_COLS * T::BM));
+#pragma unroll 1
+            for (int c32 = 0; c32 < T::D_COLS / 32; ++c32) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + T::O_COL + c32 * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    po[(size_t)(c32 * 8 + q) * T::BM + r] =
+                        make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            }
+            float* ml = a.part_ml + (size_t)w.piece * 2 * T::BM;
+            ml[r] = m;
+            ml[T::BM + r] = l;
+            tc_fence_before();
+            mbar_arrive_warp(smem_u32(&aux->bar_odrained));
+            split_arrive<T>(a, w, aux, wc);
+            return true;
+        }
+    }
     float lf, mf;
     int h, row;   // this row's query head and position
     wide_row<T>(a, w, r, h, row);
@@ -707,13 +760,13 @@ __device__ bool wide_correction_unit(const CUtensorMap* tm_o32, const PrefillArg
     return true;
 }
 
-template <int D, bool CAUSAL, bool PACK>
+template <int D, bool CAUSAL, bool PACK, bool SPLIT>
 __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
     prefill_kernel_wide(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_o32, const PrefillArgs args) {
-    using T = WideTraits<D, CAUSAL, PACK>;
+    using T = WideTraits<D, CAUSAL, PACK, SPLIT>;
     static_assert(sizeof(WideAux) <= T::SMEM_AUX, "auxiliary shared block too large");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -740,7 +793,9 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         mbar_init(smem_u32(&aux->bar_odrained), 4);        // 4 correction warps
         mbar_init(smem_u32(&aux->bar_tail), 1);
         mbar_init(smem_u32(&aux->bar_drain), 1);
+        mbar_init(smem_u32(&aux->bar_split_a), 4);         // 4 correction warps
         aux->abort_flag = 0;
+        aux->merge_last = 0;
         mbar_fence_init();
     }
     if (warp == T::MMA_WARP) {
@@ -761,7 +816,7 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         int J0 = 0, kq = 0;
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
-            if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
+            if (u >= wide_items<T>(args) || ld_volatile_shared(wc.abort_flag) != 0) break;
             const PrefillWork w = wide_work<T>(args, u);
             if (w.n_max <= 0) continue;
             if (!wide_softmax_unit<T>(wg, args, w, aux, tmem, wc, J0, kq, tr)) break;
@@ -773,10 +828,19 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
         int J0 = 0, kq = 0;
         for (int i = 0;; ++i) {
             const int u = persist_unit(i, x, G);
-            if (u >= args.n_full || ld_volatile_shared(wc.abort_flag) != 0) break;
+            if (u >= wide_items<T>(args) || ld_volatile_shared(wc.abort_flag) != 0) break;
             const PrefillWork w = wide_work<T>(args, u);
             if (w.n_max <= 0) {
-                wide_write_empty<T>(args, w);
+                if (T::SPLIT && w.piece >= 0) {
+                    // a piece without keys: an empty partial result (merged
+                    // as no term) still counts as an arrival
+                    const int r = (warp & 3) * 32 + (threadIdx.x & 31);
+                    args.part_ml[(size_t)w.piece * 2 * T::BM + r] = -INFINITY;
+                    args.part_ml[(size_t)w.piece * 2 * T::BM + T::BM + r] = 0.f;
+                    split_arrive<T>(args, w, aux, wc);
+                } else {
+                    wide_write_empty<T>(args, w);
+                }
                 continue;
             }
             if (!wide_correction_unit<T>(&tm_o32, args, w, aux, tmem, sQ, wc, J0, kq)) break;
@@ -799,6 +863,12 @@ __global__ void __launch_bounds__(WideTraits<D>::THREADS, 1)
     if (warp == T::MMA_WARP) {
         tc_fence_after();
         tmem_dealloc(tmem, T::TMEM_COLS);
+    }
+    // the last piece of a split unit to arrive merges it, on all threads
+    if constexpr (SPLIT) {
+        if (aux->merge_last != 0 && ld_volatile_shared(wc.abort_flag) == 0)
+            merge_unit<T>(args, aux->merge_unit[0], aux->merge_unit[1], aux->merge_unit[2],
+                          aux->merge_unit[3], (int)threadIdx.x, T::THREADS);
     }
 }
 

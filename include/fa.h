@@ -140,16 +140,14 @@ fa_status fa_fwd_prefill_ex(const void *q, const void *k, const void *v, void *o
  * Same arguments as fa_fwd_prefill; sq must be 1..FA_DECODE_MAX_SQ and
  * head_dim one of 64, 128, 256.  The partials live in a workspace that the
  * call allocates and frees stream-ordered (cudaMallocAsync/cudaFreeAsync on
- * `stream`).  At head_dim 128 with R = (hq / hkv) * sq >= 32 query rows per
- * key/value head (several queries of a GQA group) and enough of them
- * (U * R >= 1024, U the units of the packed launch as
- * fa_debug_prefill_plan_gqa reports them in out[0]), this call and
+ * `stream`).  At head_dim 128 with (hq / hkv) * sq >= 32 query rows per
+ * key/value head (several queries of a GQA group), this call and
  * fa_fwd_decode_ex without a window run the prefill kernel with the group's
  * query heads packed into one tile instead (the same result as
- * fa_fwd_prefill / fa_fwd_prefill_ex, bit for bit; no workspace): past 16
- * rows per key/value head the split kernel is bound by its tensor-core
- * work, the packed kernel by HBM, as long as its units (never split along
- * the keys) fill the GPU.  fa_fwd_decode_splits, the paged and the
+ * fa_fwd_prefill / fa_fwd_prefill_ex, bit for bit; it allocates a workspace
+ * only when it splits its units along the keys): past 16 rows per
+ * key/value head the split kernel is bound by its tensor-core work, the
+ * packed kernel by HBM.  fa_fwd_decode_splits, the paged and the
  * no-allocation entry points always run the split kernel.
  */
 fa_status fa_fwd_decode(const void *q, const void *k, const void *v, void *o,
@@ -382,13 +380,16 @@ fa_status fa_debug_prefill_trace(unsigned long long *buf, int block);
  * sequences of fa_fwd_prefill_varlen (sq is then the largest query length).
  * A unit is one (batch entry, query head, query block of out[3] rows); it
  * visits nk = ceil(sk / out[4]) key blocks; at head_dim 512 it runs as two
- * CTAs and is never split.  out[5] == 1: min(out[0], num_sms) persistent
- * CTAs process the out[0] units in turn (the 256-key kernel of head_dim 96 /
- * 128, and head_dim 256 when nothing is split).  Otherwise the grid's first
- * out[0] CTAs each process a whole unit, and the remaining out[1] units (the
- * last partial wave) are each processed by out[2] CTAs, piece i taking key
- * blocks [i nk / out[2], (i + 1) nk / out[2]); the last piece to finish
- * merges the pieces' partial results.  out: int[6]
+ * CTAs and is never split.  out[5] == 1: min(out[0] + out[1] * out[2],
+ * num_sms) persistent CTAs process the work in turn (the 256-key kernel of
+ * head_dim 96 / 128, and head_dim 256 when nothing is split); the 256-key
+ * kernel splits only when its non-causal units fill at most half the SMs
+ * (out[0] = 0: every unit in out[2] pieces of >= 4 key blocks, one piece per
+ * CTA).  Otherwise the grid's first out[0] CTAs each process a whole unit,
+ * and the remaining out[1] units (the last partial wave) are each processed
+ * by out[2] CTAs.  Piece i of a unit takes key blocks [i nk / out[2],
+ * (i + 1) nk / out[2]); the last piece to finish merges the pieces' partial
+ * results.  out: int[6]
  *   out[0] n_full, out[1] n_tail, out[2] split, out[3] query rows of a unit
  *   (128 or 256), out[4] keys of a score block (128 or 256), out[5]
  *   persistent.

@@ -130,20 +130,18 @@ def test_packed_many_units_and_repeats():
 
 DECODE_ROUTED = [
     # B, Hq, Hkv, Sq, Sk, lengths, causal, sinks: R = (Hq / Hkv) * Sq >= 32
-    # rows per kv head and packed units x R >= 1024
+    # rows per kv head
     (8, 32, 4, 4, 3000, (1, 3000), True, False),        # 32 units x 32 rows
     (4, 64, 8, 16, 2048, None, False, True),            # 32 x 128
     (6, 16, 2, 16, 5000, [5000, 0, 1, 4999, 2500, 17], True, True),   # 12 x 128
     (12, 32, 2, 2, 700, None, False, False),            # G = 16: 48 x 32
+    (1, 64, 8, 8, 9000, (1, 9000), False, True),        # one sequence: 8 units split along the keys
 ]
 
 
 def _routed(B, Hq, Hkv, Sq, Sk, causal):
-    from attention_forward_blackwell_gb300 import binding
-    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    rows = Hq // Hkv * Sq
-    units = binding.debug_prefill_plan_gqa(B, Hq, Hkv, Sq, Sk, 128, causal, n_sms).n_full
-    return rows >= 32 and units * rows >= 1024
+    """Whether fa_fwd_decode takes the packed prefill kernel (head_dim 128)."""
+    return Hq // Hkv * Sq >= 32
 
 
 @pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,lengths,causal,sinks_on", DECODE_ROUTED,

@@ -55,8 +55,16 @@ def test_plan_invariants(shape, kind, sms):
     nk = math.ceil(sk / p.keys_per_block)
     assert p.n_full + p.n_tail == units
     if wide:
-        # persistent, whole units
-        assert p.persistent and (p.n_full, p.n_tail, p.split) == (units, 0, 1)
+        # persistent; whole units, except that at most half a wave of
+        # non-causal units is split into k pieces of >= 4 key blocks, one
+        # piece per CTA
+        assert p.persistent
+        k = min(sms // units, 8, nk // 4) if (not causal and units * 2 <= sms) else 1
+        if k >= 2:
+            assert (p.n_full, p.n_tail, p.split) == (0, units, k)
+            assert units * k <= sms
+        else:
+            assert (p.n_full, p.n_tail, p.split) == (units, 0, 1)
         return
     assert p.persistent == (d == 256 and not packed and p.n_tail == 0 and p.n_full > 0)
     if p.split == 1:
@@ -146,3 +154,15 @@ def test_gqa_plan_rejects_bad_group():
         binding.debug_prefill_plan_gqa(1, 6, 4, 16, 128, 128, False, 152)
     with pytest.raises(binding.FaError):
         binding.debug_prefill_plan_gqa(1, 6, 0, 16, 128, 128, False, 152)
+
+
+@pytest.mark.parametrize("shape,want", [
+    ((1, 2, 300, 5000, 128, False), (0, 6, 5)),       # 6 units of 20 key blocks: 5 pieces each
+    ((1, 1, 128, 65536, 96, False), (0, 1, 8)),       # one unit: 8 pieces
+    ((1, 2, 300, 5000, 128, True), (6, 0, 1)),        # causal units are never split
+    ((1, 2, 300, 1500, 128, False), (6, 0, 1)),       # 6 key blocks: pieces would be too short
+    ((2, 40, 128, 8192, 128, False), (80, 0, 1)),     # more than half a wave
+])
+def test_few_units_of_the_256_key_kernel_are_split(shape, want):
+    batch, hq, sq, sk, d, causal = shape
+    assert tuple(binding.debug_prefill_plan_ex(batch, hq, sq, sk, d, causal, 152))[:3] == want

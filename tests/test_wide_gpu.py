@@ -222,3 +222,77 @@ def test_random_shapes_every_element(B, Hq, Hkv, Sq, Sk, d, causal, lengths):
     ro, rl = oracle_for(x, scale, causal)
     compare(o, lse, ro, rl, f"random {B, Hq, Hkv, Sq, Sk, d} causal={causal} lengths={lengths}")
     free_cuda()
+
+
+SPLIT = [
+    # B, Hq, Hkv, Sq, Sk, d, lengths: at most half a wave of units, each cut
+    # along the keys into pieces of >= 4 key blocks over several CTAs
+    (1, 2, 2, 300, 5000, 128, None),               # 6 units x 5 pieces
+    (1, 1, 1, 128, 65536, 96, None),               # one unit x 8 pieces
+    (2, 2, 1, 200, 6000, 128, [6000, 1100]),       # later pieces of a short sequence: no key
+    (1, 4, 2, 129, 4097, 96, None),                # ragged: a last block of one key
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk,d,lengths", SPLIT,
+                         ids=[f"b{c[0]}h{c[1]}q{c[3]}k{c[4]}d{c[5]}" for c in SPLIT])
+def test_split_units_every_element(B, Hq, Hkv, Sq, Sk, d, lengths):
+    """Pieces write unnormalised O, row max and row sum to scratch; the last
+    to arrive merges them (rebasing each to the common max) and stores O and
+    LSE."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = _assert_wide(B, Hq, Sq, Sk, d)
+    assert p.n_full == 0 and p.split > 1 and p.n_tail * p.split <= n_sms, p
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=2100 + Sq + Sk, device="cuda",
+                           lengths=lengths)
+    if lengths is not None:
+        inputs.poison_beyond_lengths(x.k, x.seqlens_k)
+        inputs.poison_beyond_lengths(x.v, x.seqlens_k)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(x, scale)
+    ro, rl = oracle_for(x, scale, False)
+    compare(o, lse, ro, rl, f"split {B, Hq, Hkv, Sq, Sk, d} x{p.split} lengths={lengths}")
+    free_cuda()
+
+
+def test_split_units_with_sinks_packed_and_replayed():
+    """Head-packed units split along the keys (4 units of 8 heads x 16
+    queries, 8 pieces each), with sinks; bit-equal over repeated launches and
+    a CUDA graph replay (the arrival counters reset themselves)."""
+    from attention_forward_blackwell_gb300 import binding, inputs
+    B, Hq, Hkv, Sq, Sk, d = 1, 32, 4, 16, 8192, 128
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    p = binding.debug_prefill_plan_gqa(B, Hq, Hkv, Sq, Sk, d, False, n_sms)
+    assert p.pack == 8 and p.n_full == 0 and p.n_tail == 4 and p.split == 8, p
+    x = inputs.make_inputs(B, Hq, Hkv, Sq, Sk, d, tag=2200, device="cuda")
+    g = torch.Generator().manual_seed(29)
+    sinks = (2.0 * torch.randn(Hq, generator=g)).float().cuda()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(x, scale, sinks=sinks)
+    ro, rl = oracle.attention_fwd(inputs.bf16_bits(x.q), inputs.bf16_bits(x.k),
+                                  inputs.bf16_bits(x.v), scale=scale, causal=False,
+                                  threads=THREADS, sinks=sinks.cpu().double().numpy())
+    compare(o, lse, ro, rl, "packed split with sinks")
+    for _ in range(3):
+        o2, l2 = _run(x, scale, sinks=sinks)
+        assert torch.equal(o, o2) and torch.equal(lse, l2)
+    o3 = torch.empty_like(o)
+    l3 = torch.empty_like(lse)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        binding.prefill(x.q, x.k, x.v, scale=scale, sinks=sinks, out=o3, lse=l3)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        binding.prefill(x.q, x.k, x.v, scale=scale, sinks=sinks, out=o3, lse=l3)
+    for _ in range(3):
+        o3.zero_()
+        l3.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        check_device_error()
+        assert torch.equal(o3, o) and torch.equal(l3, lse)
+    free_cuda()
