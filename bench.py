@@ -63,12 +63,12 @@ KERNEL_SOURCES = {
 
 CAPTURED_TRAFFIC = {
     # kernel: (sources sha256, workload, bytes per launch)
-    "prefill": ("ed8a858fdd4f4a1e7517b6b1b935445e69996749c6f4db5a6c067e6dc34057b6",
-                "long_prefill_b1_h16_s8192_d128", 115893504),
-    # captured at batch 16 (463.66 MB, 1.017 x its algorithmic bytes) and
+    "prefill": ("2c87fe4f574f485b478774c76ac76c261f8ae7a5bb32e1582f47bd86ef6e07af",
+                "long_prefill_b1_h16_s8192_d128", 115617024),
+    # captured at batch 16 (463.73 MB, 1.017 x its algorithmic bytes) and
     # scaled to batch 64 by the algorithmic bytes of the two batches
-    "decode": ("6ff7d2c6ac0365ca5fd8b80ea2e46d75363b1b86b70345db738ab9a9aead4b3f",
-               "decode_gqa_b64_hq64_hkv8_d128", 2205418853),
+    "decode": ("4f0491259b04d4788454cb2e2704a1707995117770ea3398451eb287333e470e",
+               "decode_gqa_b64_hq64_hkv8_d128", 2205759804),
 }
 
 
