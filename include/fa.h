@@ -92,10 +92,12 @@ typedef enum fa_status {
  * queries (sq <= 64) that kernel packs the query heads of a kv group into
  * one 128-row tile (P heads x 128 / P positions, P a power of two dividing
  * hq / hkv: see fa_debug_prefill_plan_gqa), so that they share each K/V tile
- * ("b200-flash-attention4-planner" E.7, head-packed GQA).  For the other
+ * ("b200-flash-attention4-planner" E.7, head-packed GQA); when its
+ * non-causal units fill at most half the SMs, it cuts each into 2-8 pieces
+ * along the key axis, one per CTA, merged on the device.  For the other
  * non-causal problems the query blocks of the last, partial wave are split
  * along the key axis over several CTAs and merged on the device (see
- * fa_debug_prefill_plan_ex),
+ * fa_debug_prefill_plan_ex); a split launch
  * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
  * with cudaFreeAsync on the same stream) of at most SMs * 130 KB (head_dim
  * 128; in proportion for other head dims).
