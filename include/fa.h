@@ -97,8 +97,8 @@ typedef enum fa_status {
  * along the key axis, one per CTA, merged on the device.  For the other
  * non-causal problems the query blocks of the last, partial wave are split
  * along the key axis over several CTAs and merged on the device (see
- * fa_debug_prefill_plan_ex); a split launch
- * which takes a stream-ordered scratch allocation (cudaMallocAsync, freed
+ * fa_debug_prefill_plan_ex).  A split launch
+ * takes a stream-ordered scratch allocation (cudaMallocAsync, freed
  * with cudaFreeAsync on the same stream) of at most SMs * 130 KB (head_dim
  * 128; in proportion for other head dims).
  * Sizes: batch, hq, hkv, sq, sk >= 0 (any zero size is a no-op returning
