@@ -104,5 +104,11 @@ CHUNKED_GQA = Workload("chunked_prefill_gqa_b64_hq32_hkv4_q16_k4096_d128", 64, 3
                        description="chunked prefill GQA B=64 Hq=32 Hkv=4 Sq=16 Sk=4096 d=128 "
                                    "causal")
 
+# few units over long keys (32 units of 128 rows on 152 SMs), where the
+# 256-key kernel splits each unit along the keys (not a configuration of the
+# pages)
+SPLIT_FEW = Workload("split_prefill_b1_h8_q512_k16384_d128", 1, 8, 8, 512, 16384, 128, False, 10,
+                     description="prefill B=1 H=8 Sq=512 Sk=16384 d=128 non-causal (few units)")
+
 ALL = [TINY, PREFILL_D128, PREFILL_D128_CAUSAL, LONG_D128, LONG_D96, PREFILL_D64, GQA_D256,
-       PREFILL_D512, PREFILL_D512_CAUSAL, DECODE, CHUNKED_GQA]
+       PREFILL_D512, PREFILL_D512_CAUSAL, DECODE, CHUNKED_GQA, SPLIT_FEW]
