@@ -166,3 +166,20 @@ def test_gqa_plan_rejects_bad_group():
 def test_few_units_of_the_256_key_kernel_are_split(shape, want):
     batch, hq, sq, sk, d, causal = shape
     assert tuple(binding.debug_prefill_plan_ex(batch, hq, sq, sk, d, causal, 152))[:3] == want
+
+
+@pytest.mark.parametrize("batch,hq,hkv,sq,sk,d,causal,want", [
+    # packed units (P heads x R rows), split along the keys when few
+    (1, 32, 4, 16, 8192, 128, False, (0, 4, 8, 16, 256, True, 8)),
+    (1, 16, 2, 8, 3000, 128, False, (0, 2, 3, 16, 256, True, 8)),
+    (64, 32, 4, 16, 4096, 128, True, (256, 0, 1, 16, 256, True, 8)),
+    (64, 32, 4, 16, 4096, 128, False, (256, 0, 1, 16, 256, True, 8)),
+    (2, 8, 2, 40, 9000, 96, False, (0, 8, 8, 64, 256, True, 2)),    # 40 queries: 64 rows per head
+    (1, 8, 8, 16, 9000, 128, False, (0, 8, 8, 128, 256, True, 1)),   # MHA: no packing
+])
+def test_packing_with_splits(batch, hq, hkv, sq, sk, d, causal, want):
+    p = binding.debug_prefill_plan_gqa(batch, hq, hkv, sq, sk, d, causal, 152)
+    assert tuple(p) == want
+    n_full, n_tail, split = want[:3]
+    assert n_full + n_tail == batch * (hq // want[6]) * math.ceil(sq / want[3])
+    assert n_tail * split <= 152
